@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Throughput of y = FP16(x . W^T) + b on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one call of poot_linear_f16 on one batch of seeded synthetic
+inputs already resident in HBM.  The default workload is the MLP
+up-projection (M=8192, N=14336, K=4096), the largest configured shape; its
+x + W + y (416 MB) exceed the 129 MB L2, so no flush is needed between
+steps.  Under torchrun (N > 1) every rank runs an independent replica on
+its own GPU (weak scaling, no data-path collective); the step time is the
+maximum over ranks.
+
+Reported beside the device-timed value:
+  roofline      the GEMM kernel's achieved TFLOP/s (algorithmic 2MNK per
+                launch / mean CUDA-event duration on its stream) against the
+                measured dense bf16 peak (the fp16 tensor rate is the same);
+                traffic = DRAM bytes per launch from the committed ncu
+                summary when it matches the current kernel source, else null
+  e2e           same metric through the C ABI with host buffers: pinned
+                host->device copies of x, W, b and device->host copy of y
+                inside the timed region
+  cpu_baseline  the CPU oracle timed on a bounded row sample on the host
+                cores (a reported baseline, not the target)
+  clocks        nvidia-smi samples taken during the timed region
+``--impl reference`` times the CPU oracle alone on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import datetime as _dt
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "TFLOP/s of y=FP16(x·Wᵀ)+b per M×N×K; % of FP16 tensor peak / HBM BW"
+CPU_SAMPLE_SECONDS = 10.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default="mlp_up")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--cpu-seconds", type=float, default=CPU_SAMPLE_SECONDS)
+    p.add_argument("--variant", default="auto", help="force a kernel variant (auto, gemm_tma, gemv, ...)")
+    a = p.parse_args()
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if a.steps < 1:
+        p.error("--steps must be >= 1")
+    return a
+
+
+# ---- distributed plumbing (replicas only) ------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def max_over_ranks(dist, value, device):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---- peaks, clocks, profiles ----------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, reasons) with host timestamps."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for r in csv.reader(fh):
+                if len(r) < 10:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(r[2]), float(r[3]), r[4].strip(), [s.strip() for s in r[5:10]]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i in range(4) if r[4][i + 1].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_fp16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.json if it matches the source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            entries = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    src = kernel_source_hash()
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source_hash") == src:
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+# ---- CPU oracle sample ----------------------------------------------------------
+def cpu_oracle_sample(x, w, b, seconds: float, y_gpu=None):
+    """Time the oracle on a row sample sized to about `seconds` of work."""
+    import numpy as np
+    import oracle
+    M, K = x.shape
+    N = w.shape[0]
+    threads = oracle.default_threads()
+    xb = x.view(torch_int16()).numpy().view(np.uint16)
+    wb = w.view(torch_int16()).numpy().view(np.uint16)
+    bb = b.view(torch_int16()).numpy().view(np.uint16)
+    # calibrate on one row per thread
+    rows = min(M, threads)
+    t = time.perf_counter()
+    oracle.linear_f16(xb[:rows], wb, bb, nthreads=threads)
+    per_row = (time.perf_counter() - t) / rows
+    want = int(max(threads, min(M, seconds / max(per_row, 1e-9))))
+    want = min(M, want)
+    rng = np.random.default_rng(2024)
+    sample = np.sort(rng.choice(M, size=want, replace=False))
+    t = time.perf_counter()
+    y_ref = oracle.linear_f16(np.ascontiguousarray(xb[sample]), wb, bb, nthreads=threads)
+    dt = time.perf_counter() - t
+    flops = 2.0 * want * N * K
+    out = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{want} of {M} rows (seeded), all {N} columns, K={K}; {dt:.2f} s on {threads} threads",
+           "seconds": round(dt, 3)}
+    if y_gpu is not None:
+        g = y_gpu[sample]
+        same = (g == y_ref)
+        out["sample_rows_identical_bits"] = float(same.mean())
+    return out, y_ref, sample
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
+# ---- arms -----------------------------------------------------------------------
+def run_reference(args, rank, world):
+    import torch
+    from linear_fp16_gb300 import synth
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    x, w, b = synth.workload_inputs(args.workload)
+    # each step: a bounded row sample of the workload, sized so that the
+    # whole run stays within a few minutes
+    per_step = max(0.2, min(3.0, 120.0 / (args.steps + args.warmup)))
+    vals = []
+    last = None
+    for i in range(args.warmup + args.steps):
+        res, _, _ = cpu_oracle_sample(x, w, b, per_step)
+        if i >= args.warmup:
+            vals.append(res["value"])
+            last = res
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "dist": wl.dist,
+                   "seed": wl.seed, "accumulate": "f32", "sample": "rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import linear_fp16_gb300 as L
+    from linear_fp16_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    lib = L.load_library()
+
+    wl = synth.WORKLOADS[args.workload]
+    M, N, K = wl.M, wl.N, wl.K
+    x_h, w_h, b_h = synth.workload_inputs(args.workload, seed_offset=0)
+    x = x_h.to(dev)
+    w = w_h.to(dev)
+    b = b_h.to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    variant = L.VARIANT_AUTO
+    if args.variant != "auto":
+        variant = {v: k for k, v in L.VARIANT_NAMES.items()}[args.variant]
+    chosen = L.variant_for(x, w, b, y) if variant == L.VARIANT_AUTO else variant
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ptrs = (x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr())
+
+    def step():
+        rc = lib.poot_linear_f16_ex(*ptrs, M, N, K, variant, 0, sh)
+        if rc != 0:
+            raise RuntimeError(f"poot_linear_f16: {L.poot_linear_status_string(rc)}")
+
+    working_set = 2 * (M * K + N * K + N + M * N)
+    flush = None
+    if working_set <= 2 * L2_BYTES:
+        # small working set: rotate an L2-sized scratch write between steps
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+    if L.poot_linear_device_status(sh) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        if flush is not None:
+            flush.zero_()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    wall1 = time.time()
+    clocks = None
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary(wall0, wall1)
+    kernel_ms = [a.elapsed_time(bv) for a, bv in ev]
+    total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        step_ms_local = statistics.mean(kernel_ms)   # flushes are outside the step
+    else:
+        step_ms_local = total_ms / args.steps
+    step_ms = max_over_ranks(dist, step_ms_local, dev)
+    kern_ms = max_over_ranks(dist, statistics.mean(kernel_ms), dev)
+    if L.poot_linear_device_status(sh) != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+
+    flops = 2.0 * M * N * K
+    value = world * flops / (step_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers --------------------
+    e2e = None
+    if not args.no_e2e:
+        xp, wp, bp = x_h.pin_memory(), w_h.pin_memory(), b_h.pin_memory()
+        yp = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        xd, wd, bd = torch.empty_like(x), torch.empty_like(w), torch.empty_like(b)
+        yd = torch.empty_like(y)
+        pe = (xd.data_ptr(), wd.data_ptr(), bd.data_ptr(), yd.data_ptr())
+
+        def e2e_step():
+            xd.copy_(xp, non_blocking=True)
+            wd.copy_(wp, non_blocking=True)
+            bd.copy_(bp, non_blocking=True)
+            rc = lib.poot_linear_f16(*pe, M, N, K, sh)
+            if rc != 0:
+                raise RuntimeError("poot_linear_f16 failed in e2e")
+            yp.copy_(yd, non_blocking=True)
+
+        e2e_steps = max(3, min(args.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        e2e_ms = max_over_ranks(dist, a0.elapsed_time(a1) / e2e_steps, dev)
+        # the copies made it: y on the host equals y on the device
+        same = bool(torch.equal(yp, y.cpu()))
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(2 * (M * K + N * K + N)), "d2h_bytes_per_step": int(2 * M * N),
+               "ms_per_step": e2e_ms, "steps": e2e_steps, "host_y_matches_device_y": same}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel -----------------------------------
+    peaks, src = load_peaks()
+    gemm = chosen in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG)
+    kernel_name = {L.VARIANT_GEMM_TMA: "gemm_f16_tcgen05_kernel<tma>",
+                   L.VARIANT_GEMM_CPASYNC: "gemm_f16_tcgen05_kernel<cpasync4>",
+                   L.VARIANT_GEMM_REG: "gemm_f16_tcgen05_kernel<reg16>",
+                   L.VARIANT_GEMV: "gemv_f16_kernel<vec>", L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
+                   }.get(chosen, "bias_only_kernel")
+    kern_s = kern_ms * 1e-3
+    if gemm:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = flops / kern_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{src} dense bf16 burst (fp16 runs at the bf16 rate)"}
+    else:
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        achieved = wl.algorithmic_bytes / kern_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{src} STREAM-style copy"}
+    roof["traffic"] = committed_traffic(kernel_name, wl.name)
+    roof["kernel"] = kernel_name
+    roof["kernel_ms"] = kern_ms
+    roof["algorithmic_per_launch"] = flops if gemm else wl.algorithmic_bytes
+    roof["hbm_gbs_algorithmic"] = wl.algorithmic_bytes / kern_s / 1e9
+
+    cpu = None
+    if not args.no_cpu:
+        y_bits = y.cpu().view(torch.int16).numpy().view(np.uint16)
+        cpu, _, _ = cpu_oracle_sample(x_h, w_h, b_h, args.cpu_seconds, y_gpu=y_bits)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "N": N, "K": K, "dist": wl.dist, "seed": wl.seed,
+                   "accumulate": "f32", "variant": L.VARIANT_NAMES.get(chosen, str(chosen)),
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": ("inputs larger than L2 (x+W+b+y = %.0f MB > 129 MB)" % (working_set / 1e6))
+                   if flush is None else "L2 flushed between steps (512 MB write, outside the step events)",
+                   "hbm_gbs_algorithmic": wl.algorithmic_bytes / (step_ms * 1e-3) / 1e9},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

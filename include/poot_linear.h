@@ -1,0 +1,152 @@
+/*
+ * poot_linear.h -- C ABI of the GB300 (sm_103a) FP16 linear library.
+ *
+ * One operation:  y = FP16(x . W^T) + b
+ *
+ *   x  [M, K]  row-major binary16, one input row per output row
+ *   W  [N, K]  row-major binary16, [out_features, in_features]; the kernels
+ *              read it in this layout (the transpose is never formed)
+ *   b  [N]     binary16, the same b[n] for every row
+ *   y  [M, N]  row-major binary16
+ *
+ * Numerical contract ("Tensor Programs, Part 1", section "One Program and One
+ * Numerical Contract", the proj formula and rules 1-2, and the Figure 1.1
+ * caption):
+ *   1. the products x[m,k] * W[n,k] enter an FP32 sum unrounded (each product
+ *      of two binary16 numbers is exact in binary32); the summation order is
+ *      free;
+ *   2. proj[m,n] = RN16(sum) is rounded to binary16 BEFORE the bias, then
+ *      y[m,n] = RN16(proj[m,n] + b[n]).  proj lives only in registers.
+ * RN16 is IEEE round-to-nearest-even with gradual underflow and overflow to
+ * infinity.
+ *
+ * All entry points are plain C: device pointers and sizes, no torch types.
+ * All functions return a status code (POOT_OK or a POOT_ERR_* value) and
+ * never abort the process; an error is reported, not raised.
+ */
+#ifndef POOT_LINEAR_H
+#define POOT_LINEAR_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define POOT_API __attribute__((visibility("default")))
+#else
+#define POOT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t); NULL is the legacy default
+ * stream of the calling thread's current device. */
+typedef struct CUstream_st* poot_stream_t;
+
+/* ---- status codes ------------------------------------------------------- */
+enum {
+    POOT_OK = 0,
+    POOT_ERR_INVALID_ARG = 1,        /* NULL pointer, negative or too large
+                                        dimension, y overlapping an input,
+                                        an unknown or inapplicable variant */
+    POOT_ERR_MISALIGNED = 2,         /* a pointer is not 2-byte aligned */
+    POOT_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
+    POOT_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed;
+                                        poot_linear_last_cuda_error() names it */
+    POOT_ERR_DEVICE_TIMEOUT = 5      /* a kernel's bounded wait ran out */
+};
+
+/* ---- kernel variants (the plan-time GEMV / GEMM split) ------------------ */
+enum {
+    POOT_VARIANT_AUTO = -1,       /* choose from M, N, K and pointer alignment */
+    POOT_VARIANT_NONE = 0,        /* M == 0 or N == 0: nothing to do */
+    POOT_VARIANT_BIAS_ONLY = 1,   /* K == 0: y[m,n] = RN16(+0 + b[n]) */
+    POOT_VARIANT_GEMV = 2,        /* M <= 16: HBM-bound weight stream,
+                                     128-bit loads (K % 8 == 0, x and W
+                                     16-byte aligned) */
+    POOT_VARIANT_GEMV_SCALAR = 3, /* M <= 16, any K and alignment */
+    POOT_VARIANT_GEMM_TMA = 4,    /* tcgen05 GEMM, TMA loads of x and W
+                                     (K % 8 == 0, x and W 16-byte aligned) */
+    POOT_VARIANT_GEMM_CPASYNC = 5,/* tcgen05 GEMM, 4-byte async copies for
+                                     row pitches TMA cannot take
+                                     (K even, x and W 4-byte aligned) */
+    POOT_VARIANT_GEMM_REG = 6     /* tcgen05 GEMM, 2-byte register copies
+                                     (any K and alignment) */
+};
+
+/* Largest M served by the GEMV variants. */
+#define POOT_GEMV_MAX_M 16
+
+/*
+ * y = FP16(x . W^T) + b on the calling thread's current device.
+ *
+ * Source: "Tensor Programs, Part 1", the toy linear y = matmul(x, weight.T) + b
+ * and its numerical contract (section "One Program and One Numerical
+ * Contract"); the call mirrors the linear(builder, h, weight, bias) op of
+ * the poot "Tracing a Model" page.
+ *
+ * x, w, b, y: device pointers (memory of the current device) to contiguous
+ *   row-major binary16 data with the shapes above.  2-byte alignment is
+ *   required; 16-byte alignment of x, w and y (and K % 8 == 0, N % 8 == 0)
+ *   selects the TMA paths, anything else takes a slower path with the same
+ *   results.
+ * M, N, K: sizes, 0 <= M, N, K < 2^31.  M == 0 or N == 0 launches nothing
+ *   (pointers may then be NULL).  K == 0 gives y = b in every row (x and w
+ *   may then be NULL).
+ * stream: the work is queued on it; the call does not synchronise.
+ * Ownership: the caller owns all four buffers.  x, w and b are only read;
+ *   every element of y is written.  y must not overlap x, w or b.  The
+ *   library allocates nothing per call.
+ * Errors: argument errors are found before any CUDA call and nothing is
+ *   queued.  Launch failures return POOT_ERR_CUDA.  Faults inside a kernel
+ *   surface at the caller's next synchronisation, as for any CUDA kernel;
+ *   a bounded device-side wait that runs out is reported by
+ *   poot_linear_device_status().
+ */
+POOT_API int poot_linear_f16(const void* x, const void* w, const void* b, void* y,
+                    int64_t M, int64_t N, int64_t K, poot_stream_t stream);
+
+/*
+ * Same operation with an explicit variant (for tests and benchmarks).
+ * variant: POOT_VARIANT_AUTO or one of the POOT_VARIANT_* codes; a variant
+ *   whose preconditions the arguments do not meet returns
+ *   POOT_ERR_INVALID_ARG (nothing is queued).
+ * gemv_warps_per_row: 0 = automatic; 1, 2, 4 or 8 forces how many warps of
+ *   the GEMV split one output feature's K range (ignored by other variants).
+ */
+POOT_API int poot_linear_f16_ex(const void* x, const void* w, const void* b, void* y,
+                       int64_t M, int64_t N, int64_t K, int variant,
+                       int gemv_warps_per_row, poot_stream_t stream);
+
+/*
+ * The variant poot_linear_f16 would run for these arguments (pure host
+ * logic: pointers are inspected for alignment only, never dereferenced; no
+ * CUDA call).  Returns a POOT_VARIANT_* code >= 0, or -POOT_ERR_* when the
+ * arguments are invalid.
+ */
+POOT_API int poot_linear_f16_variant(const void* x, const void* w, const void* b, const void* y,
+                            int64_t M, int64_t N, int64_t K);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+POOT_API const char* poot_linear_status_string(int status);
+
+/* Name of the CUDA error behind the calling thread's last POOT_ERR_CUDA
+ * (static string; "cudaSuccess" if there was none). */
+POOT_API const char* poot_linear_last_cuda_error(void);
+
+/*
+ * Synchronises `stream`, then reports and clears the current device's
+ * device-side error word: POOT_ERR_DEVICE_TIMEOUT if a kernel's bounded
+ * wait ran out since the last call, POOT_ERR_CUDA if the synchronisation
+ * failed, else POOT_OK.
+ */
+POOT_API int poot_linear_device_status(poot_stream_t stream);
+
+/* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
+POOT_API int poot_linear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POOT_LINEAR_H */

@@ -1,0 +1,16 @@
+"""GB300-native FP16 linear: y = FP16(x . W^T) + b on sm_103a.
+
+``linear(x, w, b)`` is the tensor-level call; the C entry points of
+include/poot_linear.h are mirrored one to one in ``binding``.
+"""
+from .binding import (  # noqa: F401
+    GEMV_MAX_M, POOT_ERR_CUDA, POOT_ERR_DEVICE_TIMEOUT, POOT_ERR_INVALID_ARG,
+    POOT_ERR_MISALIGNED, POOT_ERR_UNSUPPORTED_DEVICE, POOT_OK, PootLinearError,
+    VARIANT_AUTO, VARIANT_BIAS_ONLY, VARIANT_GEMM_CPASYNC, VARIANT_GEMM_REG,
+    VARIANT_GEMM_TMA, VARIANT_GEMV, VARIANT_GEMV_SCALAR, VARIANT_NAMES, VARIANT_NONE,
+    library_path, linear, load_library, poot_linear_device_status, poot_linear_f16,
+    poot_linear_f16_ex, poot_linear_f16_variant, poot_linear_last_cuda_error,
+    poot_linear_status_string, poot_linear_version, variant_for,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,178 @@
+"""ctypes binding of libpoot_linear.so: argument marshalling only.
+
+The functions named like the C entry points (include/poot_linear.h) take raw
+device pointers and sizes and return the status code.  ``linear`` is the
+tensor-level call: it checks torch tensors, allocates y with torch, and
+calls ``poot_linear_f16`` on the current stream.  Every step of the
+computation runs in the CUDA library; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+# status codes and variants (mirror include/poot_linear.h)
+POOT_OK = 0
+POOT_ERR_INVALID_ARG = 1
+POOT_ERR_MISALIGNED = 2
+POOT_ERR_UNSUPPORTED_DEVICE = 3
+POOT_ERR_CUDA = 4
+POOT_ERR_DEVICE_TIMEOUT = 5
+
+VARIANT_AUTO = -1
+VARIANT_NONE = 0
+VARIANT_BIAS_ONLY = 1
+VARIANT_GEMV = 2
+VARIANT_GEMV_SCALAR = 3
+VARIANT_GEMM_TMA = 4
+VARIANT_GEMM_CPASYNC = 5
+VARIANT_GEMM_REG = 6
+VARIANT_NAMES = {
+    VARIANT_NONE: "none", VARIANT_BIAS_ONLY: "bias_only", VARIANT_GEMV: "gemv",
+    VARIANT_GEMV_SCALAR: "gemv_scalar", VARIANT_GEMM_TMA: "gemm_tma",
+    VARIANT_GEMM_CPASYNC: "gemm_cpasync", VARIANT_GEMM_REG: "gemm_reg",
+}
+GEMV_MAX_M = 16
+
+# (name, restype, argtypes) of every exported symbol
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+EXPORTS = {
+    "poot_linear_f16": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP]),
+    "poot_linear_f16_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int,
+                                          ctypes.c_int, _VP]),
+    "poot_linear_f16_variant": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64]),
+    "poot_linear_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "poot_linear_last_cuda_error": (ctypes.c_char_p, []),
+    "poot_linear_device_status": (ctypes.c_int, [_VP]),
+    "poot_linear_version": (ctypes.c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PootLinearError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if status == POOT_ERR_CUDA:
+            msg += f" [{last_cuda_error()}]"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the CUDA library; raise if impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library missing: {path} (run python -m linear_fp16_gb300.build)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+# ---- raw C entry points --------------------------------------------------
+def poot_linear_f16(x: int, w: int, b: int, y: int, M: int, N: int, K: int, stream: int) -> int:
+    return load_library().poot_linear_f16(x, w, b, y, M, N, K, stream)
+
+
+def poot_linear_f16_ex(x: int, w: int, b: int, y: int, M: int, N: int, K: int, variant: int,
+                       gemv_warps_per_row: int, stream: int) -> int:
+    return load_library().poot_linear_f16_ex(x, w, b, y, M, N, K, variant, gemv_warps_per_row, stream)
+
+
+def poot_linear_f16_variant(x: int, w: int, b: int, y: int, M: int, N: int, K: int) -> int:
+    return load_library().poot_linear_f16_variant(x, w, b, y, M, N, K)
+
+
+def poot_linear_status_string(status: int) -> str:
+    return load_library().poot_linear_status_string(status).decode()
+
+
+def poot_linear_last_cuda_error() -> str:
+    return load_library().poot_linear_last_cuda_error().decode()
+
+
+def poot_linear_device_status(stream: int) -> int:
+    return load_library().poot_linear_device_status(stream)
+
+
+def poot_linear_version() -> int:
+    return load_library().poot_linear_version()
+
+
+status_string = poot_linear_status_string
+last_cuda_error = poot_linear_last_cuda_error
+
+
+# ---- tensor-level call ---------------------------------------------------
+def _check(t, name, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float16:
+        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row: int = 0,
+           stream=None):
+    """y = FP16(x . W^T) + b with x [M,K], w [N,K], b [N] fp16 CUDA tensors.
+
+    Runs on ``stream`` (default: the current torch stream of x's device) and
+    returns y [M,N] (``out`` if given).  Raises PootLinearError on a status
+    other than POOT_OK.
+    """
+    import torch
+    _check(x, "x", 2)
+    _check(w, "w", 2)
+    _check(b, "b", 1)
+    M, K = x.shape
+    N, K2 = w.shape
+    if K2 != K or b.shape[0] != N:
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}, b {tuple(b.shape)}")
+    dev = x.device
+    if w.device != dev or b.device != dev:
+        raise ValueError("x, w and b must be on the same device")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", 2)
+        if tuple(out.shape) != (M, N) or out.device != dev:
+            raise ValueError("out must be [M, N] on x's device")
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream(dev) if stream is None else stream
+        rc = poot_linear_f16_ex(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
+                                M, N, K, variant, gemv_warps_per_row, s.cuda_stream)
+    if rc != POOT_OK:
+        raise PootLinearError(rc, "poot_linear_f16")
+    return out
+
+
+def variant_for(x, w, b, y) -> int:
+    """The variant the library would choose for these tensors."""
+    M, K = x.shape
+    N = w.shape[0]
+    return poot_linear_f16_variant(x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), M, N, K)

@@ -1,0 +1,398 @@
+// y = FP16(x . W^T) + b on the 5th-generation tensor cores (tcgen05).
+//
+// One persistent CTA per SM walks output tiles of BM x BN (BM = 128) in a
+// grouped order (consecutive CTAs share rows of x and W in L2).  Warp roles:
+//   warps 0-3  epilogue: TMEM -> registers (tcgen05.ld), proj = RN16(acc)
+//              (cvt.rn.f16x2.f32), y = RN16(proj + b[n]) (HADD2), staged in
+//              shared memory and written by TMA stores (or plain stores when
+//              y's pitch is not 16-byte aligned).  proj never reaches HBM.
+//   warp 4     TMEM allocator and single-thread MMA issuer: per K block of 64,
+//              four tcgen05.mma kind::f16 (M=128, N=BN, K=16) into an FP32
+//              accumulator in TMEM; two accumulators alternate so the
+//              epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 5+   producer: TMA tiles of x [128 x 64] and W [BN x 64], both
+//              K-major with the 128-byte swizzle, into a STAGES-deep ring;
+//              or, for row pitches TMA cannot address (K % 8 != 0 or
+//              unaligned pointers), four warps that copy the same swizzled
+//              layout with 4-byte cp.async or 2-byte register copies.
+// Tails in M, N and K: TMA zero-fills out-of-range reads (zeros add nothing
+// to the sum) and clips stores; the copy producers zero-fill by predicate.
+//
+// Numerical contract ("Tensor Programs, Part 1", section "One Program and One
+// Numerical Contract"): products enter an FP32 sum unrounded (the tensor
+// core forms exact products of binary16 inputs), the FP32 result is rounded
+// to FP16 before the bias is added, and y is FP16.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace poot {
+
+enum LoadMode : int { kLoadTma = 0, kLoadCpAsync4 = 1, kLoadReg16 = 2 };
+
+struct GemmArgs {
+  const __half* x;
+  const __half* w;
+  const __half* b;
+  __half* y;
+  int M, N, K;
+  int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+  int tma_store;  // 1: TMA store of y; 0: plain stores (any pitch/alignment)
+};
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;        // one 128-byte swizzle row of binary16
+constexpr int kGemmEpiWarps = 4;
+constexpr int kGemmMmaWarp = 4;
+constexpr int kGemmProdWarp0 = 5;
+constexpr int kGemmGroupM = 8;     // tile-order group height (in M blocks)
+
+__host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 4; }
+__host__ __device__ constexpr int gemm_threads(int mode) {
+  return (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
+}
+__host__ __device__ constexpr uint32_t tmem_cols_for(int bn) {
+  return (2 * bn <= 32) ? 32u : (2 * bn <= 64) ? 64u : (2 * bn <= 128) ? 128u
+       : (2 * bn <= 256) ? 256u : 512u;
+}
+
+// Shared-memory layout (offsets from a 1024-byte-aligned base).
+template <int BN, int STAGES>
+struct GemmLayout {
+  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
+  static constexpr int B_BYTES = BN * kGemmBK * 2;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES;
+  static constexpr int STG_BYTES = 32 * 32 * 2;  // one 32 x 32 output box
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_STG = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BIAS = OFF_STG + kGemmEpiWarps * 2 * STG_BYTES;
+  static constexpr int OFF_BAR = OFF_BIAS + kGemmEpiWarps * BN * 2;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr int BYTES = OFF_ABORT + 4;
+  static constexpr int DYN_BYTES = BYTES + 1024;  // room to align the base
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
+  static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte objects");
+};
+
+// Tile t -> (M block, N block): groups of kGemmGroupM M blocks are walked
+// column by column, so CTAs running at the same time share x rows and W rows.
+__device__ __forceinline__ void gemm_tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
+  const int span = kGemmGroupM * num_n;
+  const int g = t / span;
+  const int first_m = g * kGemmGroupM;
+  const int gsize = min(num_m - first_m, kGemmGroupM);
+  const int local = t - g * span;
+  mb = first_m + local % gsize;
+  nb = local / gsize;
+}
+
+// Copy producer: fills one stage (A rows m0.., B rows n0.., K block kb) in
+// the 128-byte-swizzled K-major layout, zero outside [rows) x [K).
+// Row r, 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
+template <int MODE, int ROWS>
+__device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* __restrict__ src,
+                                               int row0, int nrows, int K, int k0, int pt) {
+  if constexpr (MODE == kLoadCpAsync4) {
+    // 4-byte words: ROWS x 32 words; thread pt takes words pt, pt+128, ...
+    constexpr int WORDS = ROWS * 32;
+#pragma unroll 8
+    for (int wd = pt; wd < WORDS; wd += 128) {
+      const int r = wd >> 5, kw = wd & 31;
+      const int grow = row0 + r, k = k0 + 2 * kw;
+      const bool ok = (grow < nrows) && (k < K);  // K even: the pair is all in or all out
+      const __half* g = ok ? src + (size_t)grow * K + k : src;
+      const uint32_t d = dst_base + r * 128 + ((((kw >> 2) ^ (r & 7))) << 4) + ((kw & 3) << 2);
+      cp_async_4(d, g, ok ? 4u : 0u);
+    }
+  } else {
+    // 16-byte chunks assembled from 2-byte loads: ROWS x 8 chunks.
+    constexpr int CHUNKS = ROWS * 8;
+    constexpr int PER = CHUNKS / 128;
+    uint32_t v[PER][4];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int ch = pt + i * 128;
+      const int r = ch >> 3, c = ch & 7;
+      const int grow = row0 + r, kb = k0 + c * 8;
+      unsigned short e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool ok = (grow < nrows) && (kb + j < K);
+        e[j] = ok ? __ldg(reinterpret_cast<const unsigned short*>(src) + (size_t)grow * K + kb + j)
+                  : (unsigned short)0;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[i][j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int ch = pt + i * 128;
+      const int r = ch >> 3, c = ch & 7;
+      const uint32_t d = dst_base + r * 128 + ((c ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v[i][0]), "r"(v[i][1]),
+                   "r"(v[i][2]), "r"(v[i][3])
+                   : "memory");
+    }
+  }
+}
+
+template <int BN, int STAGES, int MODE>
+__global__ void __launch_bounds__(gemm_threads(MODE), 1)
+    gemm_f16_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x,
+                            const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_y, const GemmArgs args) {
+  using L = GemmLayout<BN, STAGES>;
+  constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
+  constexpr uint32_t IDESC = idesc_f16_f32acc(kGemmBM, BN);
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: multiple of 32 in [32, 256]");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + L::OFF_BAR;
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto bar_tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t bar_drain = bar0 + 8u * (2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), MODE == kLoadTma ? 1u : 128u);
+      mbar_init(bar_empty(s), 1u);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1u);
+      mbar_init(bar_tempty(a), (uint32_t)kGemmEpiWarps);
+    }
+    mbar_init(bar_drain, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kGemmMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  if (MODE == kLoadTma && warp == kGemmProdWarp0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 0 && lane == 0 && args.tma_store) tma_prefetch_desc(&tm_y);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_kb = args.num_k_blocks;
+
+  if (warp >= kGemmProdWarp0) {
+    // ------------------------------------------------------------ producer
+    if constexpr (MODE == kLoadTma) {
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+          int mb, nb;
+          gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+          for (int kb = 0; kb < num_kb; ++kb) {
+            if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+            const uint32_t fb = bar_full(stage);
+            mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE_TX);
+            tma_load_2d(sbase + L::OFF_A + stage * L::A_BYTES, &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
+            tma_load_2d(sbase + L::OFF_B + stage * L::B_BYTES, &tm_w, fb, kb * kGemmBK, nb * BN);
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+        // Let the last loads land before the CTA can exit (their barrier
+        // phases complete on their own; nothing else arrives there).
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+          mbar_wait(bar_full(s), ph, nullptr);
+        }
+      }
+    } else {
+      const int pt = threadIdx.x - kGemmProdWarp0 * 32;  // 0..127
+      constexpr int LAG = (MODE == kLoadCpAsync4) ? STAGES - 1 : 0;
+      long long it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const int stage = (int)(it % STAGES);
+          const uint32_t phase = (uint32_t)((it / STAGES) & 1);
+          if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          gemm_copy_tile<MODE, kGemmBM>(sbase + L::OFF_A + stage * L::A_BYTES, args.x,
+                                        mb * kGemmBM, args.M, args.K, kb * kGemmBK, pt);
+          gemm_copy_tile<MODE, BN>(sbase + L::OFF_B + stage * L::B_BYTES, args.w, nb * BN,
+                                   args.N, args.K, kb * kGemmBK, pt);
+          if constexpr (MODE == kLoadCpAsync4) {
+            cp_async_commit();
+            if (it >= LAG) {
+              cp_async_wait_group<LAG>();
+              fence_proxy_async_smem();
+              mbar_arrive(bar_full((int)((it - LAG) % STAGES)));
+            }
+          } else {
+            fence_proxy_async_smem();
+            mbar_arrive(bar_full(stage));
+          }
+          ++it;
+        }
+      }
+      if constexpr (MODE == kLoadCpAsync4) {
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        for (long long j = (it > LAG ? it - LAG : 0); j < it; ++j) mbar_arrive(bar_full((int)(j % STAGES)));
+      }
+    }
+  } else if (warp == kGemmMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + stage * L::A_BYTES);
+          const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + stage * L::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kGemmBK / 16; ++k) {
+            // advance 16 elements = 32 bytes along K inside the swizzle row
+            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(bar_empty(stage));  // frees the stage when these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(bar_tfull(acc));  // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp;  // TMEM lanes 32*ew .. 32*ew+31 = tile rows
+    __half* bias_s = reinterpret_cast<__half*>(smem + L::OFF_BIAS) + ew * BN;
+    uint8_t* stg = smem + L::OFF_STG + ew * 2 * L::STG_BYTES;
+    const uint32_t stg_addr = sbase + L::OFF_STG + ew * 2 * L::STG_BYTES;
+    int buf = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int M = args.M, N = args.N;
+    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+      const int m0 = mb * kGemmBM, n0 = nb * BN;
+      // bias of this tile into warp-private shared memory, fetched before
+      // the accumulator wait so its latency overlaps the main loop
+      __syncwarp();
+#pragma unroll
+      for (int j = lane; j < BN; j += 32) {
+        const int n = n0 + j;
+        bias_s[j] = (n < N) ? args.b[n] : __float2half_rn(0.0f);
+      }
+      __syncwarp();
+      // warp-uniform decision: the TMEM loads below are warp-collective
+      const bool got = mbar_wait(bar_tfull(acc), acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t trow = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(trow + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+        uint32_t packed[16];
+        const uint4* bv = reinterpret_cast<const uint4*>(bias_s + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 bb = bv[q];
+          const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = q * 4 + e;
+            // proj = RN16(acc) for two columns, then y = RN16(proj + b)
+            const __half2 p = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&bw[e]));
+            packed[i] = *reinterpret_cast<const uint32_t*>(&yv);
+          }
+        }
+        if (args.tma_store) {
+          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+        }
+        // row `lane` of the 32 x 32 box, 64-byte swizzle: chunk q at q ^ ((row >> 1) & 3)
+        uint8_t* rowp = stg + buf * L::STG_BYTES + lane * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int pos = q ^ ((lane >> 1) & 3);
+          *reinterpret_cast<uint4*>(rowp + pos * 16) =
+              make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        }
+        if (args.tma_store) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_y, stg_addr + buf * L::STG_BYTES, n0 + c * 32, m0 + ew * 32);
+            bulk_commit_group();
+          }
+        } else {
+          __syncwarp();
+          const uint8_t* box = stg + buf * L::STG_BYTES;
+          const int col = n0 + c * 32 + lane;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = m0 + ew * 32 + rr;
+            if (row < M && col < N) {
+              const int pos = (lane >> 3) ^ ((rr >> 1) & 3);
+              args.y[(size_t)row * N + col] =
+                  *reinterpret_cast<const __half*>(box + rr * 64 + pos * 16 + (lane & 7) * 2);
+            }
+          }
+          __syncwarp();
+        }
+        buf ^= 1;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (args.tma_store && lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kGemmMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace poot

@@ -1,0 +1,361 @@
+// C ABI of the GB300 FP16 linear library: argument checks, the plan-time
+// choice between the GEMV and GEMM kernels, TMA descriptor encoding and the
+// launches.  Declared in include/poot_linear.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "poot_linear.h"
+#include "gemm_tcgen05.cuh"
+#include "gemv.cuh"
+
+namespace {
+
+using namespace poot;
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int kMaxDevices = 64;
+
+// GEMM configuration: 128 x 256 output tiles, 4-stage operand ring.
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+using Layout = GemmLayout<kBN, kStages>;
+
+constexpr int kGemvSmemBudget = 64 * 1024;  // bytes of x staged per GEMV block
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+struct DeviceState {
+  bool ready = false;
+  int status = POOT_OK;  // POOT_OK or POOT_ERR_UNSUPPORTED_DEVICE / CUDA
+  int sm_count = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_devices[kMaxDevices];
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+EncodeTiledFn g_encode_tiled = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = e;
+  return POOT_ERR_CUDA;
+}
+
+template <int MODE>
+cudaError_t set_gemm_attrs() {
+  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<kBN, kStages, MODE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout::DYN_BYTES);
+}
+
+template <int MT, bool VEC>
+cudaError_t set_gemv_attrs() {
+  return cudaFuncSetAttribute(gemv_f16_kernel<MT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kGemvSmemBudget);
+}
+
+// One-time, per-device set-up: architecture check, SM count, kernel
+// attributes, the driver's tensor-map encoder.
+int device_state(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return POOT_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+      st.ready = true;
+      st.status = POOT_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      if (g_encode_tiled == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+        g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+      if ((e = set_gemm_attrs<kLoadTma>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadCpAsync4>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadReg16>()) != cudaSuccess ||
+          (e = set_gemv_attrs<1, true>()) != cudaSuccess || (e = set_gemv_attrs<2, true>()) != cudaSuccess ||
+          (e = set_gemv_attrs<4, true>()) != cudaSuccess || (e = set_gemv_attrs<8, true>()) != cudaSuccess ||
+          (e = set_gemv_attrs<16, true>()) != cudaSuccess ||
+          (e = set_gemv_attrs<1, false>()) != cudaSuccess ||
+          (e = set_gemv_attrs<2, false>()) != cudaSuccess ||
+          (e = set_gemv_attrs<4, false>()) != cudaSuccess ||
+          (e = set_gemv_attrs<8, false>()) != cudaSuccess ||
+          (e = set_gemv_attrs<16, false>()) != cudaSuccess)
+        return cuda_fail(e);
+      st.sm_count = sms;
+      st.status = POOT_OK;
+      st.ready = true;
+    }
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return st.status;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (a == nullptr || b == nullptr || abytes <= 0 || bbytes <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+// Argument checks shared by every entry point (no CUDA calls).
+int validate(const void* x, const void* w, const void* b, const void* y, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return POOT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return POOT_OK;
+  if (y == nullptr || b == nullptr) return POOT_ERR_INVALID_ARG;
+  if (K > 0 && (x == nullptr || w == nullptr)) return POOT_ERR_INVALID_ARG;
+  if (!aligned(y, 2) || !aligned(b, 2)) return POOT_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(x, 2) || !aligned(w, 2))) return POOT_ERR_MISALIGNED;
+  const int64_t ybytes = M * N * 2;
+  if (overlaps(y, ybytes, b, N * 2)) return POOT_ERR_INVALID_ARG;
+  if (K > 0 && (overlaps(y, ybytes, x, M * K * 2) || overlaps(y, ybytes, w, N * K * 2)))
+    return POOT_ERR_INVALID_ARG;
+  return POOT_OK;
+}
+
+bool xw_tma_ok(const void* x, const void* w, int64_t K) {
+  return K % 8 == 0 && aligned(x, 16) && aligned(w, 16);
+}
+
+int choose_variant(const void* x, const void* w, int64_t M, int64_t N, int64_t K) {
+  if (M == 0 || N == 0) return POOT_VARIANT_NONE;
+  if (K == 0) return POOT_VARIANT_BIAS_ONLY;
+  const bool tma = xw_tma_ok(x, w, K);
+  if (M <= POOT_GEMV_MAX_M) return tma ? POOT_VARIANT_GEMV : POOT_VARIANT_GEMV_SCALAR;
+  if (tma) return POOT_VARIANT_GEMM_TMA;
+  if (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) return POOT_VARIANT_GEMM_CPASYNC;
+  return POOT_VARIANT_GEMM_REG;
+}
+
+// Whether a forced variant's preconditions hold.
+bool variant_applicable(int v, const void* x, const void* w, int64_t M, int64_t N, int64_t K) {
+  const bool empty = (M == 0 || N == 0);
+  switch (v) {
+    case POOT_VARIANT_NONE: return empty;
+    case POOT_VARIANT_BIAS_ONLY: return !empty && K == 0;
+    case POOT_VARIANT_GEMV: return !empty && K > 0 && M <= POOT_GEMV_MAX_M && xw_tma_ok(x, w, K);
+    case POOT_VARIANT_GEMV_SCALAR: return !empty && K > 0 && M <= POOT_GEMV_MAX_M;
+    case POOT_VARIANT_GEMM_TMA: return !empty && K > 0 && xw_tma_ok(x, w, K);
+    case POOT_VARIANT_GEMM_CPASYNC: return !empty && K > 0 && K % 2 == 0 && aligned(x, 4) && aligned(w, 4);
+    case POOT_VARIANT_GEMM_REG: return !empty && K > 0;
+    default: return false;
+  }
+}
+
+// Row-major [outer, inner] binary16 tensor, box [box_outer, box_inner].
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
+                int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  GemmArgs a;
+  a.x = static_cast<const __half*>(x);
+  a.w = static_cast<const __half*>(w);
+  a.b = static_cast<const __half*>(b);
+  a.y = static_cast<__half*>(y);
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.num_m_blocks = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
+  a.num_n_blocks = static_cast<int>((N + kBN - 1) / kBN);
+  a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
+  const int64_t tiles = int64_t(a.num_m_blocks) * a.num_n_blocks;
+  if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
+  a.num_tiles = static_cast<int>(tiles);
+  a.tma_store = (N % 8 == 0 && aligned(y, 16)) ? 1 : 0;
+
+  CUtensorMap tx, tw, ty;
+  std::memset(&tx, 0, sizeof(tx));
+  std::memset(&tw, 0, sizeof(tw));
+  std::memset(&ty, 0, sizeof(ty));
+  if (variant == POOT_VARIANT_GEMM_TMA) {
+    if (!encode_2d(&tx, x, K, M, kGemmBK, kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, w, K, N, kGemmBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
+  switch (variant) {
+    case POOT_VARIANT_GEMM_TMA:
+      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadTma>
+          <<<grid, gemm_threads(kLoadTma), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      break;
+    case POOT_VARIANT_GEMM_CPASYNC:
+      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadCpAsync4>
+          <<<grid, gemm_threads(kLoadCpAsync4), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      break;
+    default:
+      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadReg16>
+          <<<grid, gemm_threads(kLoadReg16), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      break;
+  }
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+}
+
+template <bool VEC>
+void launch_gemv_mt(int mt, dim3 grid, size_t smem, cudaStream_t stream, const GemvArgs& a) {
+  switch (mt) {
+    case 1: gemv_f16_kernel<1, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+    case 2: gemv_f16_kernel<2, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+    case 4: gemv_f16_kernel<4, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+    case 8: gemv_f16_kernel<8, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+    default: gemv_f16_kernel<16, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+  }
+}
+
+int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
+                int64_t M, int64_t N, int64_t K, int wpr_req, cudaStream_t stream) {
+  int mt = 1;
+  while (mt < M) mt *= 2;
+  int wpr = wpr_req;
+  if (wpr == 0) {
+    // enough warps in flight to cover HBM latency: about 16 per SM
+    const int64_t target = int64_t(st.sm_count) * 16;
+    wpr = 1;
+    while (wpr < kGemvWarps && N * wpr < target) wpr *= 2;
+  }
+  // K chunk staged in shared memory: a multiple of 256 elements
+  int64_t kc = (kGemvSmemBudget / (2 * mt)) / 256 * 256;
+  const int64_t kround = (K + 255) / 256 * 256;
+  if (kc > kround) kc = kround;
+  GemvArgs a;
+  a.x = static_cast<const __half*>(x);
+  a.w = static_cast<const __half*>(w);
+  a.b = static_cast<const __half*>(b);
+  a.y = static_cast<__half*>(y);
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.wpr = wpr;
+  a.kc = static_cast<int>(kc);
+  const int rows_per_block = kGemvWarps / wpr;
+  const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
+  if (blocks > INT32_MAX) return POOT_ERR_INVALID_ARG;
+  const size_t smem = static_cast<size_t>(mt) * static_cast<size_t>(kc) * 2;
+  if (variant == POOT_VARIANT_GEMV)
+    launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
+  else
+    launch_gemv_mt<false>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+}
+
+int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K, int variant,
+        int gemv_wpr, cudaStream_t stream) {
+  int rc = validate(x, w, b, y, M, N, K);
+  if (rc != POOT_OK) return rc;
+  if (gemv_wpr != 0 && gemv_wpr != 1 && gemv_wpr != 2 && gemv_wpr != 4 && gemv_wpr != 8)
+    return POOT_ERR_INVALID_ARG;
+  if (variant == POOT_VARIANT_AUTO) {
+    variant = choose_variant(x, w, M, N, K);
+  } else if (!variant_applicable(variant, x, w, M, N, K)) {
+    return POOT_ERR_INVALID_ARG;
+  }
+  if (variant == POOT_VARIANT_NONE) return POOT_OK;
+
+  int dev = 0;
+  DeviceState* st = nullptr;
+  rc = device_state(&dev, &st);
+  if (rc != POOT_OK) return rc;
+
+  switch (variant) {
+    case POOT_VARIANT_BIAS_ONLY: {
+      const int64_t total = M * N;
+      int64_t blocks = (total + 255) / 256;
+      const int64_t cap = int64_t(st->sm_count) * 8;
+      if (blocks > cap) blocks = cap;
+      bias_only_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+          static_cast<const __half*>(b), static_cast<__half*>(y), M, N);
+      const cudaError_t e = cudaGetLastError();
+      return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+    }
+    case POOT_VARIANT_GEMV:
+    case POOT_VARIANT_GEMV_SCALAR:
+      return launch_gemv(variant, *st, x, w, b, y, M, N, K, gemv_wpr, stream);
+    default:
+      return launch_gemm(variant, *st, x, w, b, y, M, N, K, stream);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+                    poot_stream_t stream) {
+  return run(x, w, b, y, M, N, K, POOT_VARIANT_AUTO, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_f16_ex(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+                       int variant, int gemv_warps_per_row, poot_stream_t stream) {
+  if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_REG) return POOT_ERR_INVALID_ARG;
+  return run(x, w, b, y, M, N, K, variant, gemv_warps_per_row, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_f16_variant(const void* x, const void* w, const void* b, const void* y, int64_t M, int64_t N,
+                            int64_t K) {
+  const int rc = validate(x, w, b, y, M, N, K);
+  if (rc != POOT_OK) return -rc;
+  return choose_variant(x, w, M, N, K);
+}
+
+const char* poot_linear_status_string(int status) {
+  switch (status) {
+    case POOT_OK: return "ok";
+    case POOT_ERR_INVALID_ARG: return "invalid argument";
+    case POOT_ERR_MISALIGNED: return "pointer not 2-byte aligned";
+    case POOT_ERR_UNSUPPORTED_DEVICE: return "unsupported device (sm_103 required)";
+    case POOT_ERR_CUDA: return "CUDA error";
+    case POOT_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* poot_linear_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
+
+int poot_linear_device_status(poot_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, poot::g_device_error, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(poot::g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return POOT_ERR_DEVICE_TIMEOUT;
+  }
+  return POOT_OK;
+}
+
+int poot_linear_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+"""The C-ABI boundary on the CPU: exports, argument checks, variant choice.
+
+No test here needs a GPU: argument errors are detected before any CUDA
+call, and the variant choice is pure host logic.
+"""
+import os
+import re
+
+import pytest
+
+import linear_fp16_gb300 as L
+from linear_fp16_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "poot_linear.h")
+
+# fake, far-apart, 256-byte-aligned "device addresses" (never dereferenced)
+X, W, B, Y = 0x1000_0000_0, 0x2000_0000_0, 0x3000_0000_0, 0x4000_0000_0
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"POOT_API\s+[\w\s\*]+?\b(poot_\w+)\s*\(", src)
+
+
+def test_library_builds_and_loads():
+    lib = L.load_library()
+    assert os.path.exists(L.library_path())
+    assert L.poot_linear_version() == 100
+    assert lib is L.load_library()
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    names = declared_functions()
+    assert len(names) == 7, names
+    lib = L.load_library()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in binding.EXPORTS, n
+    assert set(binding.EXPORTS) == set(names)
+
+
+def test_status_strings():
+    for code in range(6):
+        s = L.poot_linear_status_string(code)
+        assert s and s != "unknown status"
+    assert L.poot_linear_status_string(99) == "unknown status"
+    assert L.poot_linear_last_cuda_error() == "cudaSuccess"
+
+
+@pytest.mark.parametrize("M,N,K,want", [
+    (1, 4096, 4096, L.VARIANT_GEMV),
+    (8, 4096, 4096, L.VARIANT_GEMV),
+    (16, 4096, 4096, L.VARIANT_GEMV),
+    (17, 4096, 4096, L.VARIANT_GEMM_TMA),
+    (1024, 1024, 768, L.VARIANT_GEMM_TMA),
+    (2047, 1000, 770, L.VARIANT_GEMM_CPASYNC),
+    (100, 100, 771, L.VARIANT_GEMM_REG),
+    (3, 10, 771, L.VARIANT_GEMV_SCALAR),
+    (3, 10, 0, L.VARIANT_BIAS_ONLY),
+    (0, 10, 5, L.VARIANT_NONE),
+    (10, 0, 5, L.VARIANT_NONE),
+])
+def test_variant_choice(M, N, K, want):
+    assert L.poot_linear_f16_variant(X, W, B, Y, M, N, K) == want
+
+
+def test_variant_choice_follows_alignment():
+    # 16-byte alignment of x and W selects TMA; 4-byte selects cp.async
+    assert L.poot_linear_f16_variant(X + 4, W, B, Y, 100, 64, 64) == L.VARIANT_GEMM_CPASYNC
+    assert L.poot_linear_f16_variant(X, W + 2, B, Y, 100, 64, 64) == L.VARIANT_GEMM_REG
+    assert L.poot_linear_f16_variant(X + 8, W, B, Y, 4, 64, 64) == L.VARIANT_GEMV_SCALAR
+    # y alignment does not change the load variant (it only picks the store path)
+    assert L.poot_linear_f16_variant(X, W, B, Y + 2, 100, 64, 64) == L.VARIANT_GEMM_TMA
+
+
+@pytest.mark.parametrize("args,code", [
+    ((X, W, B, Y, -1, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((X, W, B, Y, 4, -1, 4), L.POOT_ERR_INVALID_ARG),
+    ((X, W, B, Y, 4, 4, -1), L.POOT_ERR_INVALID_ARG),
+    ((X, W, B, Y, 1 << 31, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((X, W, B, 0, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((X, W, 0, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((0, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((X, 0, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    ((X + 1, W, B, Y, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    ((X, W + 1, B, Y, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    ((X, W, B + 1, Y, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    ((X, W, B, Y + 1, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    ((X, W, B, X + 8, 4, 4, 4), L.POOT_ERR_INVALID_ARG),     # y overlaps x
+    ((X, W, B, W - 16, 4, 4, 4), L.POOT_ERR_INVALID_ARG),    # y runs into W
+    ((X, W, B, B, 4, 4, 4), L.POOT_ERR_INVALID_ARG),         # y is b
+])
+def test_argument_errors_before_any_cuda_call(args, code):
+    assert L.poot_linear_f16(*args, 0) == code
+    assert L.poot_linear_f16_variant(*args) == -code
+    assert L.poot_linear_f16_ex(*args, L.VARIANT_AUTO, 0, 0) == code
+
+
+def test_empty_problems_need_no_pointers_and_no_device():
+    assert L.poot_linear_f16(0, 0, 0, 0, 0, 5, 5, 0) == L.POOT_OK
+    assert L.poot_linear_f16(0, 0, 0, 0, 5, 0, 5, 0) == L.POOT_OK
+
+
+def test_k_zero_needs_no_x_or_w():
+    assert L.poot_linear_f16_variant(0, 0, B, Y, 3, 4, 0) == L.VARIANT_BIAS_ONLY
+
+
+@pytest.mark.parametrize("variant,M,K,xoff", [
+    (L.VARIANT_GEMV, 17, 64, 0),          # M too large for the GEMV
+    (L.VARIANT_GEMV, 4, 66, 0),           # K % 8 != 0
+    (L.VARIANT_GEMM_TMA, 100, 64, 4),     # x not 16-byte aligned
+    (L.VARIANT_GEMM_CPASYNC, 100, 65, 0), # odd K
+    (L.VARIANT_BIAS_ONLY, 100, 64, 0),    # K != 0
+    (L.VARIANT_NONE, 100, 64, 0),         # not empty
+    (7, 100, 64, 0),                      # unknown
+    (-2, 100, 64, 0),                     # unknown
+])
+def test_inapplicable_forced_variant_is_rejected(variant, M, K, xoff):
+    assert L.poot_linear_f16_ex(X + xoff, W, B, Y, M, 64, K, variant, 0, 0) == L.POOT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("wpr", [3, 5, 16, -1])
+def test_bad_gemv_warps_per_row(wpr):
+    assert L.poot_linear_f16_ex(X, W, B, Y, 4, 64, 64, L.VARIANT_AUTO, wpr, 0) == L.POOT_ERR_INVALID_ARG
+
+
+def test_no_device_is_a_cuda_error_not_a_crash():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert L.poot_linear_f16(X, W, B, Y, 4, 64, 64, 0) == L.POOT_ERR_CUDA
+    assert L.poot_linear_last_cuda_error() != "cudaSuccess"
+
+
+def test_tensor_call_checks_types():
+    import torch
+    x = torch.zeros(2, 3, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        L.linear(x, x, torch.zeros(2, dtype=torch.float16))  # CPU tensors are refused
+    with pytest.raises(TypeError):
+        L.linear(x.float(), x, torch.zeros(2, dtype=torch.float16))

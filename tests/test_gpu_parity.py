@@ -1,0 +1,252 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every configured workload, every kernel variant, the golden fixtures, a
+sweep of ragged tiny shapes and the edge cases (K = 0, empty outputs, guard
+bands around y, unaligned pointers).  Large workloads are checked on sampled
+rows (every column of those rows, including all tile boundaries in N).
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_fp16_gb300 as L
+import oracle
+from linear_fp16_gb300 import synth
+from tests import exact
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+GEMM_VARIANTS = [L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG]
+GEMV_VARIANTS = [L.VARIANT_GEMV, L.VARIANT_GEMV_SCALAR]
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _gpu(x, w, b, variant=L.VARIANT_AUTO, wpr=0):
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    y = torch.full((x.shape[0], w.shape[0]), float("nan"), dtype=torch.float16, device=DEV)
+    L.linear(xd, wd, bd, y, variant=variant, gemv_warps_per_row=wpr)
+    torch.cuda.synchronize()
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    return _bits(y)
+
+
+def _check(x, w, b, y_bits, exact_ints=False, rows=None):
+    xs = x if rows is None else x[rows]
+    yr, pr = oracle.linear_f16(_bits(xs), _bits(w), _bits(b), want_proj=True)
+    yg = y_bits if rows is None else y_bits[rows]
+    ok, rep = compare(yg, yr, pr, exact=exact_ints)
+    assert ok, rep
+    return rep
+
+
+def _applicable(variant, M, K):
+    if variant in GEMV_VARIANTS:
+        return M <= L.GEMV_MAX_M and (variant == L.VARIANT_GEMV_SCALAR or K % 8 == 0)
+    if variant == L.VARIANT_GEMM_TMA:
+        return K % 8 == 0
+    if variant == L.VARIANT_GEMM_CPASYNC:
+        return K % 2 == 0
+    return True
+
+
+# ---- golden fixtures through every variant -----------------------------------
+@pytest.mark.parametrize("name", ["round_before_bias.txt", "fp32_accumulation.txt",
+                                  "no_product_rounding.txt", "overflow_boundary.txt",
+                                  "subnormal_rounding.txt"])
+@pytest.mark.parametrize("variant", GEMM_VARIANTS + GEMV_VARIANTS)
+def test_golden_on_gpu(name, variant):
+    x, w, b, y = exact.parse_golden(name)
+    xt, wt, bt = (torch.from_numpy(a.copy()) for a in (x, w, b))
+    if not _applicable(variant, xt.shape[0], xt.shape[1]):
+        pytest.skip("variant not applicable to this shape")
+    got = _gpu(xt, wt, bt, variant).view(np.float16).astype(np.float64)
+    assert exact.same_values(got, y), (got, y)
+
+
+# ---- configured workloads ----------------------------------------------------
+def test_toy_full():
+    x, w, b = synth.workload_inputs("toy")
+    assert L.poot_linear_f16_variant(*(t.to(DEV).data_ptr() for t in (x, w, b)), 1 << 40,
+                                     1024, 1024, 768) == L.VARIANT_GEMM_TMA
+    _check(x, w, b, _gpu(x, w, b))
+
+
+def test_ragged_exact_full_is_bit_exact():
+    x, w, b = synth.workload_inputs("ragged_exact")
+    _check(x, w, b, _gpu(x, w, b), exact_ints=True)
+
+
+@pytest.mark.parametrize("variant", GEMM_VARIANTS)
+def test_ragged_exact_every_gemm_variant_where_legal(variant):
+    x, w, b = synth.workload_inputs("ragged_exact")
+    if not _applicable(variant, 2047, 770):
+        pytest.skip("K % 8 != 0: no TMA")
+    _check(x, w, b, _gpu(x, w, b, variant), exact_ints=True)
+
+
+@pytest.mark.parametrize("name", ["gemv_m1", "gemv_m8"])
+def test_gemv_full(name):
+    x, w, b = synth.workload_inputs(name)
+    _check(x, w, b, _gpu(x, w, b))
+
+
+@pytest.mark.parametrize("name", ["gemv_m1", "gemv_m8"])
+@pytest.mark.parametrize("wpr", [1, 2, 4, 8])
+def test_gemv_warps_per_row(name, wpr):
+    x, w, b = synth.workload_inputs(name)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMV, wpr))
+
+
+def _sample_rows(M, n_random, seed):
+    fixed = {0, 1, 127, 128, 129, 255, 256, M // 2, M - 129, M - 128, M - 2, M - 1}
+    rng = np.random.default_rng(seed)
+    rnd = set(int(r) for r in rng.choice(M, size=n_random, replace=False))
+    return sorted(r for r in fixed | rnd if 0 <= r < M)
+
+
+@pytest.mark.parametrize("name", ["prefill", "mlp_up"])
+def test_large_sampled_rows(name):
+    x, w, b = synth.workload_inputs(name)
+    y = _gpu(x, w, b)
+    rows = _sample_rows(x.shape[0], 24, 7)
+    _check(x, w, b, y, rows=rows)
+    # rows not sampled must still be written (y was prefilled with NaN)
+    assert not np.isnan(y.view(np.float16)).any()
+
+
+# ---- ragged tiny sweep ---------------------------------------------------------
+SWEEP = [(M, N, K) for M in (1, 2, 7, 16, 17, 127, 129, 255) for N in (1, 8, 13, 129, 257)
+         for K in (1, 7, 8, 9, 16, 63, 64, 65, 136)]
+
+
+@pytest.mark.parametrize("variant", GEMM_VARIANTS + GEMV_VARIANTS)
+def test_tiny_sweep_smallint_exact(variant):
+    rng_seed = 100 + variant
+    n = 0
+    for (M, N, K) in SWEEP:
+        if not _applicable(variant, M, K):
+            continue
+        x, w, b = synth.make_inputs(M, N, K, "smallint", rng_seed + M * 7 + N * 3 + K)
+        _check(x, w, b, _gpu(x, w, b, variant), exact_ints=True)
+        n += 1
+    assert n > 0
+
+
+@pytest.mark.parametrize("variant", [L.VARIANT_AUTO] + GEMM_VARIANTS)
+def test_tiny_sweep_normal(variant):
+    for (M, N, K) in SWEEP[::3]:
+        if variant != L.VARIANT_AUTO and not _applicable(variant, M, K):
+            continue
+        x, w, b = synth.make_inputs(M, N, K, "normal", 500 + M + N + K)
+        _check(x, w, b, _gpu(x, w, b, variant))
+
+
+def test_many_tiles_long_k():
+    # several M and N tiles, K spanning many K blocks and a tail
+    x, w, b = synth.make_inputs(300, 600, 1000, "normal", 77)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA if 1000 % 8 == 0 else L.VARIANT_AUTO))
+    x, w, b = synth.make_inputs(300, 600, 1002, "smallint", 78)
+    for v in (L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG):
+        _check(x, w, b, _gpu(x, w, b, v), exact_ints=True)
+
+
+def test_more_tiles_than_sms():
+    # forces the persistent loop to take several tiles per CTA and both
+    # TMEM accumulators
+    x, w, b = synth.make_inputs(2048, 5120, 128, "smallint", 79)
+    _check(x, w, b, _gpu(x, w, b), exact_ints=True)
+
+
+# ---- edge cases ------------------------------------------------------------------
+def test_k_zero_is_bias():
+    b = torch.tensor([1.5, -2.0, -0.0, 65504.0], dtype=torch.float16)
+    x = torch.zeros((3, 0), dtype=torch.float16)
+    w = torch.zeros((4, 0), dtype=torch.float16)
+    y = _gpu(x, w, b)
+    want = np.broadcast_to(_bits(b), (3, 4)).copy()
+    want[:, 2] = 0  # +0 + -0 = +0
+    assert np.array_equal(y, want)
+
+
+def test_empty_outputs_launch_nothing():
+    x = torch.zeros((0, 5), dtype=torch.float16, device=DEV)
+    w = torch.zeros((4, 5), dtype=torch.float16, device=DEV)
+    b = torch.zeros((4,), dtype=torch.float16, device=DEV)
+    y = L.linear(x, w, b)
+    assert y.shape == (0, 4)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (200, 136, 72), (33, 1001, 40)])
+def test_guard_bands_untouched(M, N, K):
+    # y lives inside a larger buffer whose margins hold a sentinel
+    x, w, b = synth.make_inputs(M, N, K, "smallint", 90 + M)
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345.0, dtype=torch.float16, device=DEV)
+    y = buf[pad:pad + M * N].view(M, N)
+    L.linear(x.to(DEV), w.to(DEV), b.to(DEV), y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345.0) and torch.all(buf[pad + M * N:] == 12345.0)
+    _check(x, w, b, _bits(y), exact_ints=True)
+
+
+@pytest.mark.parametrize("M", [5, 300])
+def test_unaligned_pointers_take_the_ragged_paths(M):
+    N, K = 72, 64
+    x, w, b = synth.make_inputs(M, N, K, "smallint", 91 + M)
+    xs = torch.zeros(M * K + 1, dtype=torch.float16, device=DEV)
+    ws = torch.zeros(N * K + 3, dtype=torch.float16, device=DEV)
+    xd = xs[1:].view(M, K)
+    wd = ws[3:].view(N, K)
+    xd.copy_(x)
+    wd.copy_(w)
+    y = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    v = L.variant_for(xd, wd, b, y)
+    assert v in (L.VARIANT_GEMV_SCALAR, L.VARIANT_GEMM_REG)
+    L.linear(xd, wd, b.to(DEV), y)
+    torch.cuda.synchronize()
+    _check(x, w, b, _bits(y), exact_ints=True)
+
+
+def test_odd_n_uses_plain_stores():
+    x, w, b = synth.make_inputs(257, 1003, 128, "normal", 92)
+    _check(x, w, b, _gpu(x, w, b))
+
+
+def test_nonfinite_inputs_propagate():
+    x, w, b = synth.make_inputs(130, 16, 16, "smallint", 93)
+    x[3, 5] = float("inf")
+    x[7, 2] = float("nan")
+    y = _gpu(x, w, b).view(np.float16)
+    assert np.isnan(y[7]).all()
+    row3 = y[3]
+    wcol = w[:, 5].float().numpy()
+    for n in range(16):
+        if wcol[n] > 0:
+            assert np.isposinf(row3[n])
+        elif wcol[n] < 0:
+            assert np.isneginf(row3[n])
+        else:
+            assert np.isnan(row3[n])  # inf * 0
+
+
+def test_repeated_calls_are_deterministic():
+    x, w, b = synth.make_inputs(512, 512, 512, "normal", 94)
+    y1 = _gpu(x, w, b)
+    y2 = _gpu(x, w, b)
+    assert np.array_equal(y1, y2)
+
+
+def test_runs_on_a_side_stream():
+    x, w, b = synth.make_inputs(256, 256, 256, "smallint", 95)
+    s = torch.cuda.Stream()
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y = L.linear(xd, wd, bd)
+    s.synchronize()
+    _check(x, w, b, _bits(y), exact_ints=True)
