@@ -106,17 +106,32 @@ enum {
 POOT_API int poot_linear_f16(const void* x, const void* w, const void* b, void* y,
                     int64_t M, int64_t N, int64_t K, poot_stream_t stream);
 
+/* Tuning knobs of poot_linear_f16_ex; zero-initialise and set what you need. */
+typedef struct poot_linear_options {
+    int variant;             /* POOT_VARIANT_AUTO (-1) or a POOT_VARIANT_* code;
+                                0 here means POOT_VARIANT_NONE, so set it */
+    int gemv_warps_per_row;  /* 0 = automatic; 1, 2, 4 or 8 warps of the GEMV
+                                split one output feature's K range.  For
+                                3 <= M <= 16 a non-zero value also selects
+                                the CUDA-core GEMV instead of the tensor-core
+                                one */
+    int gemm_tile_n;         /* 0 = automatic; else the GEMM's output tile
+                                width: a multiple of 32 in [64, 256] */
+    int gemm_group_m;        /* 0 = automatic; else the number of 128-row
+                                blocks walked together for L2 reuse (>= 1) */
+} poot_linear_options;
+
 /*
- * Same operation with an explicit variant (for tests and benchmarks).
- * variant: POOT_VARIANT_AUTO or one of the POOT_VARIANT_* codes; a variant
- *   whose preconditions the arguments do not meet returns
- *   POOT_ERR_INVALID_ARG (nothing is queued).
- * gemv_warps_per_row: 0 = automatic; 1, 2, 4 or 8 forces how many warps of
- *   the GEMV split one output feature's K range (ignored by other variants).
+ * Same operation with explicit choices (tests, benchmarks, tuning).
+ * opts: may be NULL (everything automatic).  A variant whose preconditions
+ *   the arguments do not meet, or an out-of-range knob, returns
+ *   POOT_ERR_INVALID_ARG and queues nothing.  The knobs change the work
+ *   decomposition only; every choice gives a result within the numerical
+ *   contract above.
  */
 POOT_API int poot_linear_f16_ex(const void* x, const void* w, const void* b, void* y,
-                       int64_t M, int64_t N, int64_t K, int variant,
-                       int gemv_warps_per_row, poot_stream_t stream);
+                                int64_t M, int64_t N, int64_t K,
+                                const poot_linear_options* opts, poot_stream_t stream);
 
 /*
  * The variant poot_linear_f16 would run for these arguments (pure host

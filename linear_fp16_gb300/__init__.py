@@ -4,7 +4,7 @@
 include/poot_linear.h are mirrored one to one in ``binding``.
 """
 from .binding import (  # noqa: F401
-    GEMV_MAX_M, POOT_ERR_CUDA, POOT_ERR_DEVICE_TIMEOUT, POOT_ERR_INVALID_ARG,
+    GEMV_MAX_M, Options, options, POOT_ERR_CUDA, POOT_ERR_DEVICE_TIMEOUT, POOT_ERR_INVALID_ARG,
     POOT_ERR_MISALIGNED, POOT_ERR_UNSUPPORTED_DEVICE, POOT_OK, PootLinearError,
     VARIANT_AUTO, VARIANT_BIAS_ONLY, VARIANT_GEMM_CPASYNC, VARIANT_GEMM_REG,
     VARIANT_GEMM_TMA, VARIANT_GEMV, VARIANT_GEMV_SCALAR, VARIANT_NAMES, VARIANT_NONE,

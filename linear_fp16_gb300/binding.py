@@ -37,13 +37,26 @@ VARIANT_NAMES = {
 }
 GEMV_MAX_M = 16
 
+
+
+class Options(ctypes.Structure):
+    """struct poot_linear_options (include/poot_linear.h)."""
+    _fields_ = [("variant", ctypes.c_int), ("gemv_warps_per_row", ctypes.c_int),
+                ("gemm_tile_n", ctypes.c_int), ("gemm_group_m", ctypes.c_int)]
+
+
+def options(variant: int = -1, gemv_warps_per_row: int = 0, gemm_tile_n: int = 0,
+            gemm_group_m: int = 0) -> Options:
+    return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m)
+
+
 # (name, restype, argtypes) of every exported symbol
 _VP = ctypes.c_void_p
 _I64 = ctypes.c_int64
 EXPORTS = {
     "poot_linear_f16": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP]),
-    "poot_linear_f16_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int,
-                                          ctypes.c_int, _VP]),
+    "poot_linear_f16_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64,
+                                          ctypes.POINTER(Options), _VP]),
     "poot_linear_f16_variant": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64]),
     "poot_linear_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "poot_linear_last_cuda_error": (ctypes.c_char_p, []),
@@ -93,9 +106,10 @@ def poot_linear_f16(x: int, w: int, b: int, y: int, M: int, N: int, K: int, stre
     return load_library().poot_linear_f16(x, w, b, y, M, N, K, stream)
 
 
-def poot_linear_f16_ex(x: int, w: int, b: int, y: int, M: int, N: int, K: int, variant: int,
-                       gemv_warps_per_row: int, stream: int) -> int:
-    return load_library().poot_linear_f16_ex(x, w, b, y, M, N, K, variant, gemv_warps_per_row, stream)
+def poot_linear_f16_ex(x: int, w: int, b: int, y: int, M: int, N: int, K: int, opts, stream: int) -> int:
+    """opts: an Options instance or None (everything automatic)."""
+    ref = ctypes.byref(opts) if opts is not None else None
+    return load_library().poot_linear_f16_ex(x, w, b, y, M, N, K, ref, stream)
 
 
 def poot_linear_f16_variant(x: int, w: int, b: int, y: int, M: int, N: int, K: int) -> int:
@@ -138,7 +152,7 @@ def _check(t, name, ndim):
 
 
 def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row: int = 0,
-           stream=None):
+           gemm_tile_n: int = 0, gemm_group_m: int = 0, stream=None):
     """y = FP16(x . W^T) + b with x [M,K], w [N,K], b [N] fp16 CUDA tensors.
 
     Runs on ``stream`` (default: the current torch stream of x's device) and
@@ -164,8 +178,9 @@ def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row
             raise ValueError("out must be [M, N] on x's device")
     with torch.cuda.device(dev):
         s = torch.cuda.current_stream(dev) if stream is None else stream
-        rc = poot_linear_f16_ex(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
-                                M, N, K, variant, gemv_warps_per_row, s.cuda_stream)
+        rc = poot_linear_f16_ex(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
+                                options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m),
+                                s.cuda_stream)
     if rc != POOT_OK:
         raise PootLinearError(rc, "poot_linear_f16")
     return out

@@ -36,70 +36,77 @@ struct GemmArgs {
   const __half* b;
   __half* y;
   int M, N, K;
+  int bn;       // output tile width: multiple of 32 in [64, 256] (the MMA's N)
+  int stages;   // operand ring depth, 4 .. kGemmMaxStages
+  int group_m;  // tile-order group height in M blocks
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int tma_store;  // 1: TMA store of y; 0: plain stores (any pitch/alignment)
 };
 
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;        // one 128-byte swizzle row of binary16
+constexpr int kGemmMaxBN = 256;
+constexpr int kGemmMaxStages = 8;
 constexpr int kGemmEpiWarps = 4;
 constexpr int kGemmMmaWarp = 4;
 constexpr int kGemmProdWarp0 = 5;
-constexpr int kGemmGroupM = 8;     // tile-order group height (in M blocks)
+constexpr uint32_t kGemmTmemCols = 2 * kGemmMaxBN;  // two accumulators, 256 columns apart
 
 __host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 4; }
 __host__ __device__ constexpr int gemm_threads(int mode) {
   return (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
 }
-__host__ __device__ constexpr uint32_t tmem_cols_for(int bn) {
-  return (2 * bn <= 32) ? 32u : (2 * bn <= 64) ? 64u : (2 * bn <= 128) ? 128u
-       : (2 * bn <= 256) ? 256u : 512u;
-}
 
-// Shared-memory layout (offsets from a 1024-byte-aligned base).
-template <int BN, int STAGES>
+// Shared-memory layout (offsets from a 1024-byte-aligned base).  The operand
+// ring holds `stages` stages of A [128 x 64] followed by B [bn x 64]; every
+// stage and both tiles start on 1024-byte boundaries (bn % 8 == 0).
 struct GemmLayout {
-  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
-  static constexpr int B_BYTES = BN * kGemmBK * 2;
-  static constexpr int STAGE_TX = A_BYTES + B_BYTES;
-  static constexpr int STG_BYTES = 32 * 32 * 2;  // one 32 x 32 output box
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_STG = OFF_B + STAGES * B_BYTES;
+  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;             // 16 KB
+  static constexpr int RING_BYTES = 192 * 1024;
+  static constexpr int STG_BYTES = 32 * 32 * 2;                     // one 32 x 32 output box
+  static constexpr int OFF_STG = RING_BYTES;
   static constexpr int OFF_BIAS = OFF_STG + kGemmEpiWarps * 2 * STG_BYTES;
-  static constexpr int OFF_BAR = OFF_BIAS + kGemmEpiWarps * BN * 2;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+  static constexpr int OFF_BAR = OFF_BIAS + kGemmEpiWarps * kGemmMaxBN * 2;
+  static constexpr int NUM_BARS = 2 * kGemmMaxStages + 5;  // full, empty, tfull x2, tempty x2, drain
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int BYTES = OFF_ABORT + 4;
   static constexpr int DYN_BYTES = BYTES + 1024;  // room to align the base
-  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
   static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte objects");
 };
 
-// Tile t -> (M block, N block): groups of kGemmGroupM M blocks are walked
-// column by column, so CTAs running at the same time share x rows and W rows.
-__device__ __forceinline__ void gemm_tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
-  const int span = kGemmGroupM * num_n;
+__host__ __device__ constexpr int gemm_b_bytes(int bn) { return bn * kGemmBK * 2; }
+__host__ __device__ constexpr int gemm_stage_bytes(int bn) { return GemmLayout::A_BYTES + gemm_b_bytes(bn); }
+__host__ __device__ constexpr int gemm_max_stages(int bn) {
+  return GemmLayout::RING_BYTES / gemm_stage_bytes(bn) < kGemmMaxStages
+             ? GemmLayout::RING_BYTES / gemm_stage_bytes(bn) : kGemmMaxStages;
+}
+
+// Tile t -> (M block, N block): groups of group_m M blocks are walked column
+// by column, so CTAs running at the same time share x rows and W rows in L2.
+__device__ __forceinline__ void gemm_tile_coords(int t, int num_m, int num_n, int group_m, int& mb,
+                                                 int& nb) {
+  const int span = group_m * num_n;
   const int g = t / span;
-  const int first_m = g * kGemmGroupM;
-  const int gsize = min(num_m - first_m, kGemmGroupM);
+  const int first_m = g * group_m;
+  const int gsize = min(num_m - first_m, group_m);
   const int local = t - g * span;
   mb = first_m + local % gsize;
   nb = local / gsize;
 }
 
-// Copy producer: fills one stage (A rows m0.., B rows n0.., K block kb) in
-// the 128-byte-swizzled K-major layout, zero outside [rows) x [K).
-// Row r, 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
-template <int MODE, int ROWS>
+// Copy producer: fills one operand tile (rows row0 .. row0+rows-1 of src,
+// K block at k0) in the 128-byte-swizzled K-major layout, zero outside
+// [nrows) x [K).  Row r, 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
+// pt is the thread's index among the 128 producer threads.
+template <int MODE>
 __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* __restrict__ src,
-                                               int row0, int nrows, int K, int k0, int pt) {
+                                               int rows, int row0, int nrows, int K, int k0, int pt) {
   if constexpr (MODE == kLoadCpAsync4) {
-    // 4-byte words: ROWS x 32 words; thread pt takes words pt, pt+128, ...
-    constexpr int WORDS = ROWS * 32;
+    // 4-byte words: rows x 32 words; thread pt takes words pt, pt+128, ...
+    const int words = rows * 32;
 #pragma unroll 8
-    for (int wd = pt; wd < WORDS; wd += 128) {
+    for (int wd = pt; wd < words; wd += 128) {
       const int r = wd >> 5, kw = wd & 31;
       const int grow = row0 + r, k = k0 + 2 * kw;
       const bool ok = (grow < nrows) && (k < K);  // K even: the pair is all in or all out
@@ -108,46 +115,52 @@ __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* 
       cp_async_4(d, g, ok ? 4u : 0u);
     }
   } else {
-    // 16-byte chunks assembled from 2-byte loads: ROWS x 8 chunks.
-    constexpr int CHUNKS = ROWS * 8;
-    constexpr int PER = CHUNKS / 128;
-    uint32_t v[PER][4];
+    // 16-byte chunks assembled from 2-byte loads: rows x 8 chunks, eight
+    // chunks per thread in flight at a time.
+    constexpr int PER = 8;
+    const int chunks = rows * 8;
+    for (int base = 0; base < chunks; base += 128 * PER) {
+      uint32_t v[PER][4];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int ch = pt + i * 128;
-      const int r = ch >> 3, c = ch & 7;
-      const int grow = row0 + r, kb = k0 + c * 8;
-      unsigned short e[8];
+      for (int i = 0; i < PER; ++i) {
+        const int ch = base + pt + i * 128;
+        const int r = ch >> 3, c = ch & 7;
+        const int grow = row0 + r, kb = k0 + c * 8;
+        unsigned short e[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool ok = (grow < nrows) && (kb + j < K);
-        e[j] = ok ? __ldg(reinterpret_cast<const unsigned short*>(src) + (size_t)grow * K + kb + j)
-                  : (unsigned short)0;
+        for (int j = 0; j < 8; ++j) {
+          const bool ok = (ch < chunks) && (grow < nrows) && (kb + j < K);
+          e[j] = ok ? __ldg(reinterpret_cast<const unsigned short*>(src) + (size_t)grow * K + kb + j)
+                    : (unsigned short)0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[i][j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[i][j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
-    }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int ch = pt + i * 128;
-      const int r = ch >> 3, c = ch & 7;
-      const uint32_t d = dst_base + r * 128 + ((c ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v[i][0]), "r"(v[i][1]),
-                   "r"(v[i][2]), "r"(v[i][3])
-                   : "memory");
+      for (int i = 0; i < PER; ++i) {
+        const int ch = base + pt + i * 128;
+        if (ch < chunks) {
+          const int r = ch >> 3, c = ch & 7;
+          const uint32_t d = dst_base + r * 128 + ((c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v[i][0]), "r"(v[i][1]),
+                       "r"(v[i][2]), "r"(v[i][3])
+                       : "memory");
+        }
+      }
     }
   }
 }
 
-template <int BN, int STAGES, int MODE>
+template <int MODE>
 __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     gemm_f16_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x,
                             const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_y, const GemmArgs args) {
-  using L = GemmLayout<BN, STAGES>;
-  constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
-  constexpr uint32_t IDESC = idesc_f16_f32acc(kGemmBM, BN);
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: multiple of 32 in [32, 256]");
+  using L = GemmLayout;
+  const int BN = args.bn;
+  const int STAGES = args.stages;
+  const int STAGE_BYTES = gemm_stage_bytes(BN);
+  const uint32_t IDESC = idesc_f16_f32acc(kGemmBM, (uint32_t)BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -155,10 +168,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto bar_tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t bar_drain = bar0 + 8u * (2 * STAGES + 4);
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kGemmMaxStages + s); };
+  auto bar_tfull = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + a); };
+  auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + 2 + a); };
+  const uint32_t bar_drain = bar0 + 8u * (2 * kGemmMaxStages + 4);
+  auto stage_a = [&](int s) { return sbase + (uint32_t)(s * STAGE_BYTES); };
+  auto stage_b = [&](int s) { return sbase + (uint32_t)(s * STAGE_BYTES + L::A_BYTES); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
 
@@ -179,7 +194,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     fence_mbar_init();
   }
   if (warp == kGemmMmaWarp) {
-    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_alloc(smem_addr(tmem_slot), kGemmTmemCols);
     tmem_relinquish_alloc_permit();
   }
   if (MODE == kLoadTma && warp == kGemmProdWarp0 && lane == 0) {
@@ -204,13 +219,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         bool ok = true;
         for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
           int mb, nb;
-          gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+          gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t fb = bar_full(stage);
-            mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE_TX);
-            tma_load_2d(sbase + L::OFF_A + stage * L::A_BYTES, &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
-            tma_load_2d(sbase + L::OFF_B + stage * L::B_BYTES, &tm_w, fb, kb * kGemmBK, nb * BN);
+            mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+            tma_load_2d(stage_a(stage), &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
+            tma_load_2d(stage_b(stage), &tm_w, fb, kb * kGemmBK, nb * BN);
             ++issued;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
@@ -226,20 +241,21 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       }
     } else {
       const int pt = threadIdx.x - kGemmProdWarp0 * 32;  // 0..127
-      constexpr int LAG = (MODE == kLoadCpAsync4) ? STAGES - 1 : 0;
+      // copies of a stage complete LAG iterations after they are issued;
+      // LAG < STAGES (STAGES >= 4) keeps the ring from deadlocking
+      constexpr int LAG = (MODE == kLoadCpAsync4) ? 3 : 0;
       long long it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
-        gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+        gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
           const int stage = (int)(it % STAGES);
           const uint32_t phase = (uint32_t)((it / STAGES) & 1);
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          gemm_copy_tile<MODE, kGemmBM>(sbase + L::OFF_A + stage * L::A_BYTES, args.x,
-                                        mb * kGemmBM, args.M, args.K, kb * kGemmBK, pt);
-          gemm_copy_tile<MODE, BN>(sbase + L::OFF_B + stage * L::B_BYTES, args.w, nb * BN,
-                                   args.N, args.K, kb * kGemmBK, pt);
+          gemm_copy_tile<MODE>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K,
+                               kb * kGemmBK, pt);
+          gemm_copy_tile<MODE>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
           if constexpr (MODE == kLoadCpAsync4) {
             cp_async_commit();
             if (it >= LAG) {
@@ -271,12 +287,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
         if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kGemmMaxBN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + stage * L::A_BYTES);
-          const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + stage * L::B_BYTES);
+          const uint64_t adesc = sdesc_kmajor_sw128(stage_a(stage));
+          const uint64_t bdesc = sdesc_kmajor_sw128(stage_b(stage));
 #pragma unroll
           for (int k = 0; k < kGemmBK / 16; ++k) {
             // advance 16 elements = 32 bytes along K inside the swizzle row
@@ -297,7 +313,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp;  // TMEM lanes 32*ew .. 32*ew+31 = tile rows
-    __half* bias_s = reinterpret_cast<__half*>(smem + L::OFF_BIAS) + ew * BN;
+    __half* bias_s = reinterpret_cast<__half*>(smem + L::OFF_BIAS) + ew * kGemmMaxBN;
     uint8_t* stg = smem + L::OFF_STG + ew * 2 * L::STG_BYTES;
     const uint32_t stg_addr = sbase + L::OFF_STG + ew * 2 * L::STG_BYTES;
     int buf = 0;
@@ -306,12 +322,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     const int M = args.M, N = args.N;
     for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
       int mb, nb;
-      gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, mb, nb);
+      gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       const int m0 = mb * kGemmBM, n0 = nb * BN;
       // bias of this tile into warp-private shared memory, fetched before
       // the accumulator wait so its latency overlaps the main loop
       __syncwarp();
-#pragma unroll
       for (int j = lane; j < BN; j += 32) {
         const int n = n0 + j;
         bias_s[j] = (n < N) ? args.b[n] : __float2half_rn(0.0f);
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       const bool got = mbar_wait(bar_tfull(acc), acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const uint32_t trow = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t trow = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kGemmMaxBN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -391,7 +406,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   __syncthreads();
   if (warp == kGemmMmaWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, kGemmTmemCols);
   }
 }
 

@@ -153,6 +153,204 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_f16_kernel(const GemvArgs a
   }
 }
 
+// M <= 2, 16-byte path: one warp per W row (or per K slice of a row when
+// N is small), no shared-memory staging and no block barrier on the way.
+// For each chunk of 32 * kGemvRowVpl vectors a lane issues all its W loads
+// (16-byte vector v = chunk base + u * 32 + lane) before using any, then
+// reads the matching x vectors through the read-only path (L2 once per SM,
+// then L1) and accumulates in FP32.  On GB300 this streams W at about the
+// rate of a plain read of the same bytes.
+constexpr int kGemvRowWarps = 4;
+constexpr int kGemvRowThreads = kGemvRowWarps * 32;
+constexpr int kGemvRowVpl = 16;  // vectors per lane per chunk (16 * 32 * 8 = 4096 elements)
+
+template <int MT>
+__global__ void __launch_bounds__(kGemvRowThreads) gemv_f16_rows_kernel(const GemvArgs a) {
+  __shared__ float red[kGemvRowWarps][MT];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wpr = a.wpr;
+  const int row = blockIdx.x * (kGemvRowWarps / wpr) + warp / wpr;
+  const int part = warp % wpr;
+  const bool active = row < a.N;
+  const int nvec = a.K >> 3;
+  // this warp's contiguous slice of the row, in whole chunks of 32 vectors
+  const int segs = (nvec + 31) >> 5;
+  const int seg_per_part = (segs + wpr - 1) / wpr;
+  const int v_begin = min(nvec, part * seg_per_part * 32);
+  const int v_end = min(nvec, (part + 1) * seg_per_part * 32);
+  const uint4* __restrict__ wv = reinterpret_cast<const uint4*>(a.w + (size_t)(active ? row : 0) * a.K);
+  const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(a.x);
+
+  float acc[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+  // b[row] is fetched now, beside the first W loads, not after the sum
+  const __half bn = (active && part == 0) ? a.b[row] : __float2half_rn(0.0f);
+
+  auto fma_vec = [&](const uint4 wvec, int v) {
+    float wf[8];
+    unpack8(wvec, wf);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {  // MT == M here (M <= 2)
+      float xf[8];
+      unpack8(__ldg(xv + (size_t)m * nvec + v), xf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[m] = fmaf(wf[j], xf[j], acc[m]);
+    }
+  };
+  if (active) {
+    int c0 = v_begin;
+    // whole chunks: no per-vector guards
+    for (; c0 + 32 * kGemvRowVpl <= v_end; c0 += 32 * kGemvRowVpl) {
+      uint4 wr[kGemvRowVpl];
+#pragma unroll
+      for (int u = 0; u < kGemvRowVpl; ++u) wr[u] = ldg_stream_16(wv + c0 + u * 32 + lane);
+#pragma unroll
+      for (int u = 0; u < kGemvRowVpl; ++u) fma_vec(wr[u], c0 + u * 32 + lane);
+    }
+    // tail: batches of four guarded vectors per lane
+    for (; c0 < v_end; c0 += 32 * 4) {
+      uint4 wr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = c0 + u * 32 + lane;
+        wr[u] = (v < v_end) ? ldg_stream_16(wv + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = c0 + u * 32 + lane;
+        if (v < v_end) fma_vec(wr[u], v);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+  }
+  if (wpr > 1) {
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) red[warp][m] = acc[m];
+    }
+    __syncthreads();
+    if (part == 0) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float s = red[warp][m];
+        for (int j = 1; j < wpr; ++j) s += red[warp + j][m];
+        acc[m] = s;
+      }
+    }
+  }
+  if (part == 0 && active) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (lane == m && m < a.M) {
+        const __half p = __float2half_rn(acc[m]);  // proj, rounded before the bias
+        a.y[(size_t)m * a.N + row] = __hadd(p, bn);
+      }
+    }
+  }
+}
+
+// 3 <= M <= 16, 16-byte path, on the tensor cores (mma.sync m16n8k16, FP16
+// inputs, FP32 accumulators): on CUDA cores this range is bound by the
+// FP32 FMAs, not by HBM.  A block owns a 16-row tile of W; its eight warps
+// split K.  Per step of 32 along K, lane (g = lane / 4, t = lane % 4) loads
+// the 16-byte vectors W[n0+g][k+8t .. +8), W[n0+g+8][k+8t .. +8) and
+// x[g][k+8t .. +8) (and x[g+8][..] when M > 8).  The summation order is free
+// (the contract's rule 1), so the K index inside a step is permuted: with
+// that permutation these registers are exactly the A (W) and B (x^T)
+// fragments of two m16n8k16 MMAs, and no shuffles are needed.  D[n][m]
+// accumulates y^T; warps meet in shared memory in a fixed order.
+constexpr int kGemvMmaWarps = 8;
+constexpr int kGemvMmaThreads = kGemvMmaWarps * 32;
+
+__device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16)
+template <int NT>
+__global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const GemvArgs a) {
+  __shared__ float red[kGemvMmaWarps][32][4 * NT];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int n0 = blockIdx.x * 16;
+  const int K = a.K, N = a.N, M = a.M;
+  const int nA = n0 + g, nB = n0 + g + 8;
+  // this warp's K slice, a multiple of 32
+  const int slice = ((K + kGemvMmaWarps * 32 - 1) / (kGemvMmaWarps * 32)) * 32;
+  const int k_begin = min(K, warp * slice);
+  const int k_end = min(K, k_begin + slice);
+  const __half* __restrict__ wa = a.w + (size_t)(nA < N ? nA : 0) * K;
+  const __half* __restrict__ wb = a.w + (size_t)(nB < N ? nB : 0) * K;
+  const __half* __restrict__ x0 = a.x + (size_t)(g < M ? g : 0) * K;
+  const __half* __restrict__ x1 = a.x + (size_t)(g + 8 < M ? g + 8 : 0) * K;
+  const bool okA = nA < N, okB = nB < N, okx0 = g < M, okx1 = (NT > 1) && (g + 8 < M);
+  // bias of this lane's two output features, fetched early
+  const float bA = (warp == 0 && okA) ? __half2float(a.b[nA]) : 0.0f;
+  const float bB = (warp == 0 && okB) ? __half2float(a.b[nB]) : 0.0f;
+
+  float d[NT][4];
+#pragma unroll
+  for (int q = 0; q < NT; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+
+  constexpr int U = 4;  // steps of 32 along K per batch
+  for (int k0 = k_begin; k0 < k_end; k0 += 32 * U) {
+    uint4 va[U], vb[U], vx[U][NT];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = k0 + 32 * u + 8 * t;
+      const bool in = k < k_end;  // K % 8 == 0: whole vector in or out
+      va[u] = (in && okA) ? ldg_stream_16(wa + k) : zero;
+      vb[u] = (in && okB) ? ldg_stream_16(wb + k) : zero;
+      vx[u][0] = (in && okx0) ? __ldg(reinterpret_cast<const uint4*>(x0 + k)) : zero;
+      if (NT > 1) vx[u][NT - 1] = (in && okx1) ? __ldg(reinterpret_cast<const uint4*>(x1 + k)) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        mma_16816_f16_f32(d[q], va[u].x, vb[u].x, va[u].y, vb[u].y, vx[u][q].x, vx[u][q].y);
+        mma_16816_f16_f32(d[q], va[u].z, vb[u].z, va[u].w, vb[u].w, vx[u][q].z, vx[u][q].w);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int q = 0; q < NT; ++q)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[warp][lane][4 * q + i] = d[q][i];
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int q = 0; q < NT; ++q) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float s = red[0][lane][4 * q + i];
+      for (int wi = 1; wi < kGemvMmaWarps; ++wi) s += red[wi][lane][4 * q + i];
+      // D[n][m]: i = 0, 1 -> (n = nA, m = 2t + i); i = 2, 3 -> (n = nB, m = 2t + i - 2)
+      const int m = 8 * q + 2 * t + (i & 1);
+      const int n = (i < 2) ? nA : nB;
+      if (m < M && n < N) {
+        const __half p = __float2half_rn(s);  // proj, rounded before the bias
+        a.y[(size_t)m * N + n] = __hadd(p, __float2half_rn(i < 2 ? bA : bB));
+      }
+    }
+  }
+}
+
 // K == 0: the sum is +0, so y[m, n] = RN16(+0 + b[n]) (a -0 bias gives +0).
 __global__ void bias_only_kernel(const __half* __restrict__ b, __half* __restrict__ y, long long M,
                                  long long N) {

@@ -20,10 +20,7 @@ constexpr int kVersion = 100;  // 0.1.0
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr int kMaxDevices = 64;
 
-// GEMM configuration: 128 x 256 output tiles, 4-stage operand ring.
-constexpr int kBN = 256;
-constexpr int kStages = 4;
-using Layout = GemmLayout<kBN, kStages>;
+using Layout = GemmLayout;
 
 constexpr int kGemvSmemBudget = 64 * 1024;  // bytes of x staged per GEMV block
 
@@ -47,8 +44,8 @@ int cuda_fail(cudaError_t e) {
 
 template <int MODE>
 cudaError_t set_gemm_attrs() {
-  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<kBN, kStages, MODE>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout::DYN_BYTES);
+  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Layout::DYN_BYTES);
 }
 
 template <int MT, bool VEC>
@@ -171,8 +168,46 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+struct GemmPlan {
+  int bn, stages, group_m;
+};
+
+// Tile plan from a cost model: each CTA runs ceil(tiles / SMs) tiles; a
+// tile costs num_kb K blocks of max(MMA cycles, shared-memory operand
+// cycles) / efficiency plus a fixed pipeline fill / drain.  MMA 128 x bn x 64
+// takes 2 * bn cycles; its operands (16 KB + 128 * bn bytes) stream at about
+// 128 B/cycle.  The efficiencies of narrower tiles (more x re-reads, more
+// epilogue work per FLOP) were measured on GB300 for 224 (0.90 - 0.97) and
+// extrapolated below it.  Ties go to the wider tile.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int group_req) {
+  const int64_t num_m = (M + kGemmBM - 1) / kGemmBM;
+  const int64_t num_kb = (K + kGemmBK - 1) / kGemmBK;
+  int best_bn = 256;
+  int64_t best = INT64_MAX;
+  static const int cands[] = {256, 224, 192, 160, 128, 96, 64};
+  static const int eff_pct[] = {100, 93, 88, 83, 78, 70, 60};
+  for (int i = 0; i < 7; ++i) {
+    const int bn = cands[i];
+    if (bn_req != 0 && bn != bn_req) continue;
+    const int64_t tiles = num_m * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t per_kb = (2 * bn > 128 + bn) ? 2 * bn : 128 + bn;
+    const int64_t cost = waves * (num_kb * per_kb * 100 / eff_pct[i] + 2000);
+    if (cost < best) { best = cost; best_bn = bn; }
+  }
+  if (bn_req != 0) best_bn = bn_req;
+  GemmPlan p;
+  p.bn = best_bn;
+  p.stages = gemm_max_stages(best_bn);
+  // tiles are walked in groups of 8 M blocks (1024 rows of x); measured on
+  // GB300 to beat groups of 16, 32 and 64 on 4096^3 and 8192x14336x4096
+  p.group_m = group_req > 0 ? group_req : 8;
+  return p;
+}
+
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
-                int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+                int64_t M, int64_t N, int64_t K, int bn_req, int group_req, cudaStream_t stream) {
+  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, bn_req, group_req);
   GemmArgs a;
   a.x = static_cast<const __half*>(x);
   a.w = static_cast<const __half*>(w);
@@ -181,8 +216,11 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
+  a.bn = plan.bn;
+  a.stages = plan.stages;
+  a.group_m = plan.group_m;
   a.num_m_blocks = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
-  a.num_n_blocks = static_cast<int>((N + kBN - 1) / kBN);
+  a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
   a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
   const int64_t tiles = int64_t(a.num_m_blocks) * a.num_n_blocks;
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
@@ -195,7 +233,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   std::memset(&ty, 0, sizeof(ty));
   if (variant == POOT_VARIANT_GEMM_TMA) {
     if (!encode_2d(&tx, x, K, M, kGemmBK, kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tw, w, K, N, kGemmBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_2d(&tw, w, K, N, kGemmBK, static_cast<uint32_t>(plan.bn), CU_TENSOR_MAP_SWIZZLE_128B))
       return cuda_fail(cudaErrorInvalidValue);
   }
   if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -204,16 +242,14 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
   switch (variant) {
     case POOT_VARIANT_GEMM_TMA:
-      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadTma>
-          <<<grid, gemm_threads(kLoadTma), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      gemm_f16_tcgen05_kernel<kLoadTma><<<grid, gemm_threads(kLoadTma), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
       break;
     case POOT_VARIANT_GEMM_CPASYNC:
-      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadCpAsync4>
+      gemm_f16_tcgen05_kernel<kLoadCpAsync4>
           <<<grid, gemm_threads(kLoadCpAsync4), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
       break;
     default:
-      gemm_f16_tcgen05_kernel<kBN, kStages, kLoadReg16>
-          <<<grid, gemm_threads(kLoadReg16), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      gemm_f16_tcgen05_kernel<kLoadReg16><<<grid, gemm_threads(kLoadReg16), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
       break;
   }
   const cudaError_t e = cudaGetLastError();
@@ -260,7 +296,21 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
   if (blocks > INT32_MAX) return POOT_ERR_INVALID_ARG;
   const size_t smem = static_cast<size_t>(mt) * static_cast<size_t>(kc) * 2;
-  if (variant == POOT_VARIANT_GEMV)
+  if (variant == POOT_VARIANT_GEMV && mt <= 2 && wpr <= kGemvRowWarps) {
+    const int rpb = kGemvRowWarps / wpr;
+    const unsigned rblocks = static_cast<unsigned>((N + rpb - 1) / rpb);
+    if (mt == 1)
+      gemv_f16_rows_kernel<1><<<rblocks, kGemvRowThreads, 0, stream>>>(a);
+    else
+      gemv_f16_rows_kernel<2><<<rblocks, kGemvRowThreads, 0, stream>>>(a);
+  } else if (variant == POOT_VARIANT_GEMV && wpr_req == 0) {
+    // 3 <= M <= 16 on the tensor cores, 16 rows of W per block
+    const unsigned mblocks = static_cast<unsigned>((N + 15) / 16);
+    if (M <= 8)
+      gemv_f16_mma_kernel<1><<<mblocks, kGemvMmaThreads, 0, stream>>>(a);
+    else
+      gemv_f16_mma_kernel<2><<<mblocks, kGemvMmaThreads, 0, stream>>>(a);
+  } else if (variant == POOT_VARIANT_GEMV)
     launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
   else
     launch_gemv_mt<false>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
@@ -268,12 +318,18 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
 
-int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K, int variant,
-        int gemv_wpr, cudaStream_t stream) {
+int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+        const poot_linear_options& o, cudaStream_t stream) {
   int rc = validate(x, w, b, y, M, N, K);
   if (rc != POOT_OK) return rc;
+  int variant = o.variant;
+  const int gemv_wpr = o.gemv_warps_per_row;
+  if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_REG) return POOT_ERR_INVALID_ARG;
   if (gemv_wpr != 0 && gemv_wpr != 1 && gemv_wpr != 2 && gemv_wpr != 4 && gemv_wpr != 8)
     return POOT_ERR_INVALID_ARG;
+  if (o.gemm_tile_n != 0 && (o.gemm_tile_n < 64 || o.gemm_tile_n > kGemmMaxBN || o.gemm_tile_n % 32 != 0))
+    return POOT_ERR_INVALID_ARG;
+  if (o.gemm_group_m < 0) return POOT_ERR_INVALID_ARG;
   if (variant == POOT_VARIANT_AUTO) {
     variant = choose_variant(x, w, M, N, K);
   } else if (!variant_applicable(variant, x, w, M, N, K)) {
@@ -301,7 +357,7 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
     case POOT_VARIANT_GEMV_SCALAR:
       return launch_gemv(variant, *st, x, w, b, y, M, N, K, gemv_wpr, stream);
     default:
-      return launch_gemm(variant, *st, x, w, b, y, M, N, K, stream);
+      return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, stream);
   }
 }
 
@@ -311,13 +367,19 @@ extern "C" {
 
 int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
                     poot_stream_t stream) {
-  return run(x, w, b, y, M, N, K, POOT_VARIANT_AUTO, 0, reinterpret_cast<cudaStream_t>(stream));
+  poot_linear_options o;
+  std::memset(&o, 0, sizeof(o));
+  o.variant = POOT_VARIANT_AUTO;
+  return run(x, w, b, y, M, N, K, o, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int poot_linear_f16_ex(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
-                       int variant, int gemv_warps_per_row, poot_stream_t stream) {
-  if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_REG) return POOT_ERR_INVALID_ARG;
-  return run(x, w, b, y, M, N, K, variant, gemv_warps_per_row, reinterpret_cast<cudaStream_t>(stream));
+                       const poot_linear_options* opts, poot_stream_t stream) {
+  poot_linear_options o;
+  std::memset(&o, 0, sizeof(o));
+  o.variant = POOT_VARIANT_AUTO;
+  if (opts != nullptr) o = *opts;
+  return run(x, w, b, y, M, N, K, o, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int poot_linear_f16_variant(const void* x, const void* w, const void* b, const void* y, int64_t M, int64_t N,

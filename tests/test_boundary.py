@@ -94,7 +94,8 @@ def test_variant_choice_follows_alignment():
 def test_argument_errors_before_any_cuda_call(args, code):
     assert L.poot_linear_f16(*args, 0) == code
     assert L.poot_linear_f16_variant(*args) == -code
-    assert L.poot_linear_f16_ex(*args, L.VARIANT_AUTO, 0, 0) == code
+    assert L.poot_linear_f16_ex(*args, L.options(), 0) == code
+    assert L.poot_linear_f16_ex(*args, None, 0) == code
 
 
 def test_empty_problems_need_no_pointers_and_no_device():
@@ -117,12 +118,24 @@ def test_k_zero_needs_no_x_or_w():
     (-2, 100, 64, 0),                     # unknown
 ])
 def test_inapplicable_forced_variant_is_rejected(variant, M, K, xoff):
-    assert L.poot_linear_f16_ex(X + xoff, W, B, Y, M, 64, K, variant, 0, 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_linear_f16_ex(X + xoff, W, B, Y, M, 64, K, L.options(variant), 0) == L.POOT_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("wpr", [3, 5, 16, -1])
 def test_bad_gemv_warps_per_row(wpr):
-    assert L.poot_linear_f16_ex(X, W, B, Y, 4, 64, 64, L.VARIANT_AUTO, wpr, 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_linear_f16_ex(X, W, B, Y, 4, 64, 64, L.options(gemv_warps_per_row=wpr), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("tile_n", [32, 48, 100, 288, -64])
+def test_bad_gemm_tile_width(tile_n):
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_tile_n=tile_n), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
+def test_bad_gemm_group():
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_group_m=-1), 0) == \
+        L.POOT_ERR_INVALID_ARG
 
 
 def test_no_device_is_a_cuda_error_not_a_crash():

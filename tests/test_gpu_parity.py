@@ -13,7 +13,7 @@ import linear_fp16_gb300 as L
 import oracle
 from linear_fp16_gb300 import synth
 from tests import exact
-from tests.parity import compare
+from tests.parity import compare, legal_interval
 
 pytestmark = pytest.mark.gpu
 
@@ -26,10 +26,11 @@ def _bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def _gpu(x, w, b, variant=L.VARIANT_AUTO, wpr=0):
+def _gpu(x, w, b, variant=L.VARIANT_AUTO, wpr=0, tile_n=0, group_m=0):
     xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
     y = torch.full((x.shape[0], w.shape[0]), float("nan"), dtype=torch.float16, device=DEV)
-    L.linear(xd, wd, bd, y, variant=variant, gemv_warps_per_row=wpr)
+    L.linear(xd, wd, bd, y, variant=variant, gemv_warps_per_row=wpr, gemm_tile_n=tile_n,
+             gemm_group_m=group_m)
     torch.cuda.synchronize()
     assert L.poot_linear_device_status(0) == L.POOT_OK
     return _bits(y)
@@ -39,8 +40,12 @@ def _check(x, w, b, y_bits, exact_ints=False, rows=None):
     xs = x if rows is None else x[rows]
     yr, pr = oracle.linear_f16(_bits(xs), _bits(w), _bits(b), want_proj=True)
     yg = y_bits if rows is None else y_bits[rows]
-    ok, rep = compare(yg, yr, pr, exact=exact_ints)
+    interval = None
+    if not exact_ints:
+        interval = legal_interval(xs.numpy(), w.numpy(), b.numpy())
+    ok, rep = compare(yg, yr, pr, exact=exact_ints, interval=interval)
     assert ok, rep
+    print(rep)
     return rep
 
 
@@ -153,6 +158,23 @@ def test_many_tiles_long_k():
     x, w, b = synth.make_inputs(300, 600, 1002, "smallint", 78)
     for v in (L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG):
         _check(x, w, b, _gpu(x, w, b, v), exact_ints=True)
+
+
+@pytest.mark.parametrize("tile_n", [64, 96, 128, 160, 192, 224, 256])
+@pytest.mark.parametrize("variant", GEMM_VARIANTS)
+def test_every_tile_width(tile_n, variant):
+    # ragged N against each tile width; K spans several K blocks and a tail
+    M, N, K = 300, 700, 200 if variant != L.VARIANT_GEMM_REG else 203
+    x, w, b = synth.make_inputs(M, N, K, "smallint", 60 + tile_n)
+    if not _applicable(variant, M, K):
+        pytest.skip("variant not applicable")
+    _check(x, w, b, _gpu(x, w, b, variant, tile_n=tile_n), exact_ints=True)
+
+
+@pytest.mark.parametrize("group_m", [1, 2, 3, 8, 64])
+def test_tile_order_groups(group_m):
+    x, w, b = synth.make_inputs(1100, 900, 96, "smallint", 70 + group_m)
+    _check(x, w, b, _gpu(x, w, b, tile_n=128, group_m=group_m), exact_ints=True)
 
 
 def test_more_tiles_than_sms():
