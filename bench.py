@@ -416,10 +416,11 @@ def run_ours(args, rank, world, local):
     # ---- roofline of the dominant kernel -----------------------------------
     peaks, src = load_peaks()
     gemm = chosen in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG)
+    gemv_vec = "gemv_f16_rows_kernel" if M <= 2 else "gemv_f16_mma_kernel"
     kernel_name = {L.VARIANT_GEMM_TMA: "gemm_f16_tcgen05_kernel<tma>",
                    L.VARIANT_GEMM_CPASYNC: "gemm_f16_tcgen05_kernel<cpasync4>",
                    L.VARIANT_GEMM_REG: "gemm_f16_tcgen05_kernel<reg16>",
-                   L.VARIANT_GEMV: "gemv_f16_kernel<vec>", L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
+                   L.VARIANT_GEMV: gemv_vec, L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
                    }.get(chosen, "bias_only_kernel")
     kern_s = kern_ms * 1e-3
     if gemm:
