@@ -64,6 +64,7 @@ def parse_args():
     p.add_argument("--tile-n", type=int, default=0, help="GEMM output tile width (0 = automatic)")
     p.add_argument("--group-m", type=int, default=0, help="GEMM tile-order group (0 = automatic)")
     p.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
+    p.add_argument("--k-chunk", type=int, default=0, help="GEMM TMEM chunk along K (0 = automatic)")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -314,7 +315,7 @@ def run_ours(args, rank, world, local):
     for _ in range(copies - 1):
         sets.append((x.clone(), w.clone(), b.clone(), torch.empty_like(y)))
     ptr_sets = [(a.data_ptr(), bb.data_ptr(), c.data_ptr(), d.data_ptr()) for (a, bb, c, d) in sets]
-    opts = L.options(variant, 0, args.tile_n, args.group_m)
+    opts = L.options(variant, 0, args.tile_n, args.group_m, args.k_chunk)
     opts_ref = __import__("ctypes").byref(opts)
 
     def step(i, stream_handle):

@@ -6,6 +6,7 @@ The library lands in linear_fp16_gb300/_build/ (git-ignored).
 from __future__ import annotations
 
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -44,11 +45,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, *SOURCES, "-o", tmp]
+    cmd = [nvcc(), *ARCH, *FLAGS, "-Xptxas=-v", "-I", INCLUDE, "-I", CSRC, *SOURCES, "-o", tmp]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or r.returncode != 0:
+        sys.stdout.write(r.stdout)
+        sys.stderr.write(r.stderr)
+    if r.returncode != 0:
+        raise subprocess.CalledProcessError(r.returncode, cmd)
     os.replace(tmp, LIB)
     return LIB
 

@@ -1,27 +1,35 @@
 // y = FP16(x . W^T) + b on the 5th-generation tensor cores (tcgen05).
 //
-// One persistent CTA per SM walks output tiles of BM x BN (BM = 128) in a
-// grouped order (consecutive CTAs share rows of x and W in L2).  Warp roles:
-//   warps 0-3  epilogue: TMEM -> registers (tcgen05.ld), proj = RN16(acc)
+// One persistent CTA per SM walks output tiles of 128 x BN in a grouped
+// order (CTAs running together share rows of x and W in L2).  Warp roles:
+//   warps 0-7  epilogue.  Warp w reads TMEM lanes 32*(w%4) .. +31 (tile
+//              rows) and owns one half of the tile's columns.  After each K
+//              chunk it moves the chunk's FP32 sums from TMEM into an FP32
+//              register accumulator (tcgen05.ld + IEEE round-to-nearest
+//              adds).  After the last chunk: proj = RN16(acc)
 //              (cvt.rn.f16x2.f32), y = RN16(proj + b[n]) (HADD2), staged in
-//              shared memory and written by TMA stores (or plain stores when
+//              shared memory and written by TMA stores (plain stores when
 //              y's pitch is not 16-byte aligned).  proj never reaches HBM.
-//   warp 4     TMEM allocator and single-thread MMA issuer: per K block of 64,
-//              four tcgen05.mma kind::f16 (M=128, N=BN, K=16) into an FP32
-//              accumulator in TMEM; two accumulators alternate so the
-//              epilogue of tile i overlaps the main loop of tile i+1.
-//   warps 5+   producer: TMA tiles of x [128 x 64] and W [BN x 64], both
-//              K-major with the 128-byte swizzle, into a STAGES-deep ring;
-//              or, for row pitches TMA cannot address (K % 8 != 0 or
-//              unaligned pointers), four warps that copy the same swizzled
-//              layout with 4-byte cp.async or 2-byte register copies.
+//   warp 8     TMEM allocator and single-thread MMA issuer: per K block of 64,
+//              four tcgen05.mma kind::f16 (M=128, N=BN, K=16) into one of two
+//              TMEM chunk buffers; a chunk is chunk_kb K blocks.
+//   warps 9+   producer: TMA tiles of x [128 x 64] and W [BN x 64], both
+//              K-major with the 128-byte swizzle, into a ring of stages; or,
+//              for row pitches TMA cannot address (K % 8 != 0 or unaligned
+//              pointers), two warps that copy the same swizzled layout with
+//              4-byte cp.async or 2-byte register copies.
 // Tails in M, N and K: TMA zero-fills out-of-range reads (zeros add nothing
 // to the sum) and clips stores; the copy producers zero-fill by predicate.
 //
 // Numerical contract ("Tensor Programs, Part 1", section "One Program and One
 // Numerical Contract"): products enter an FP32 sum unrounded (the tensor
 // core forms exact products of binary16 inputs), the FP32 result is rounded
-// to FP16 before the bias is added, and y is FP16.
+// to FP16 before the bias is added, and y is FP16.  The chunked promotion
+// keeps each tensor-core accumulation chain short: the tensor core aligns
+// addends to the running sum with truncation, so a long chain against a
+// large sum loses more than a round-to-nearest sum would; restarting every
+// chunk and adding chunk sums in IEEE FP32 keeps the result within two FP16
+// ulps of a sequential FP32 sum on cancelling sums as well.
 #pragma once
 
 #include "ptx.cuh"
@@ -36,9 +44,10 @@ struct GemmArgs {
   const __half* b;
   __half* y;
   int M, N, K;
-  int bn;       // output tile width: multiple of 32 in [64, 256] (the MMA's N)
-  int stages;   // operand ring depth, 4 .. kGemmMaxStages
-  int group_m;  // tile-order group height in M blocks
+  int bn;        // output tile width: multiple of 32 in [64, 256] (the MMA's N)
+  int stages;    // operand ring depth, 4 .. kGemmMaxStages
+  int group_m;   // tile-order group height in M blocks
+  int chunk_kb;  // K blocks accumulated in TMEM before promotion (>= 1)
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int tma_store;  // 1: TMA store of y; 0: plain stores (any pitch/alignment)
 };
@@ -47,12 +56,14 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;        // one 128-byte swizzle row of binary16
 constexpr int kGemmMaxBN = 256;
 constexpr int kGemmMaxStages = 8;
-constexpr int kGemmEpiWarps = 4;
-constexpr int kGemmMmaWarp = 4;
-constexpr int kGemmProdWarp0 = 5;
-constexpr uint32_t kGemmTmemCols = 2 * kGemmMaxBN;  // two accumulators, 256 columns apart
+constexpr int kGemmEpiWarps = 8;
+constexpr int kGemmMmaWarp = 8;
+constexpr int kGemmProdWarp0 = 9;
+constexpr int kGemmCopyThreads = 64;                 // copy producers: two warps
+constexpr uint32_t kGemmTmemCols = 2 * kGemmMaxBN;  // two chunk buffers, 256 columns apart
+constexpr int kGemmHalfCols = kGemmMaxBN / 2;        // columns per epilogue warp (max)
 
-__host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 4; }
+__host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 2; }
 __host__ __device__ constexpr int gemm_threads(int mode) {
   return (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
 }
@@ -61,18 +72,18 @@ __host__ __device__ constexpr int gemm_threads(int mode) {
 // ring holds `stages` stages of A [128 x 64] followed by B [bn x 64]; every
 // stage and both tiles start on 1024-byte boundaries (bn % 8 == 0).
 struct GemmLayout {
-  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;             // 16 KB
+  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB
   static constexpr int RING_BYTES = 192 * 1024;
-  static constexpr int STG_BYTES = 32 * 32 * 2;                     // one 32 x 32 output box
+  static constexpr int STG_BYTES = 32 * 32 * 2;          // one 32 x 32 output box
   static constexpr int OFF_STG = RING_BYTES;
-  static constexpr int OFF_BIAS = OFF_STG + kGemmEpiWarps * 2 * STG_BYTES;
-  static constexpr int OFF_BAR = OFF_BIAS + kGemmEpiWarps * kGemmMaxBN * 2;
-  static constexpr int NUM_BARS = 2 * kGemmMaxStages + 5;  // full, empty, tfull x2, tempty x2, drain
+  static constexpr int OFF_BAR = OFF_STG + kGemmEpiWarps * 2 * STG_BYTES;
+  static constexpr int NUM_BARS = 2 * kGemmMaxStages + 5;  // full, empty, cfull x2, cempty x2, drain
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int BYTES = OFF_ABORT + 4;
   static constexpr int DYN_BYTES = BYTES + 1024;  // room to align the base
   static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte objects");
+  static_assert(DYN_BYTES <= 232448, "more shared memory than a CTA can have");
 };
 
 __host__ __device__ constexpr int gemm_b_bytes(int bn) { return bn * kGemmBK * 2; }
@@ -81,6 +92,9 @@ __host__ __device__ constexpr int gemm_max_stages(int bn) {
   return GemmLayout::RING_BYTES / gemm_stage_bytes(bn) < kGemmMaxStages
              ? GemmLayout::RING_BYTES / gemm_stage_bytes(bn) : kGemmMaxStages;
 }
+// Columns of the first epilogue half (a multiple of 32); the second half
+// takes the rest.
+__host__ __device__ constexpr int gemm_half0_cols(int bn) { return ((bn / 32 + 1) / 2) * 32; }
 
 // Tile t -> (M block, N block): groups of group_m M blocks are walked column
 // by column, so CTAs running at the same time share x rows and W rows in L2.
@@ -98,15 +112,16 @@ __device__ __forceinline__ void gemm_tile_coords(int t, int num_m, int num_n, in
 // Copy producer: fills one operand tile (rows row0 .. row0+rows-1 of src,
 // K block at k0) in the 128-byte-swizzled K-major layout, zero outside
 // [nrows) x [K).  Row r, 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
-// pt is the thread's index among the 128 producer threads.
+// pt is the thread's index among the kGemmCopyThreads producer threads.
 template <int MODE>
 __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* __restrict__ src,
                                                int rows, int row0, int nrows, int K, int k0, int pt) {
+  constexpr int T = kGemmCopyThreads;
   if constexpr (MODE == kLoadCpAsync4) {
-    // 4-byte words: rows x 32 words; thread pt takes words pt, pt+128, ...
+    // 4-byte words: rows x 32 words; thread pt takes words pt, pt+T, ...
     const int words = rows * 32;
 #pragma unroll 8
-    for (int wd = pt; wd < words; wd += 128) {
+    for (int wd = pt; wd < words; wd += T) {
       const int r = wd >> 5, kw = wd & 31;
       const int grow = row0 + r, k = k0 + 2 * kw;
       const bool ok = (grow < nrows) && (k < K);  // K even: the pair is all in or all out
@@ -119,11 +134,11 @@ __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* 
     // chunks per thread in flight at a time.
     constexpr int PER = 8;
     const int chunks = rows * 8;
-    for (int base = 0; base < chunks; base += 128 * PER) {
+    for (int base = 0; base < chunks; base += T * PER) {
       uint32_t v[PER][4];
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const int ch = base + pt + i * 128;
+        const int ch = base + pt + i * T;
         const int r = ch >> 3, c = ch & 7;
         const int grow = row0 + r, kb = k0 + c * 8;
         unsigned short e[8];
@@ -138,7 +153,7 @@ __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* 
       }
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const int ch = base + pt + i * 128;
+        const int ch = base + pt + i * T;
         if (ch < chunks) {
           const int r = ch >> 3, c = ch & 7;
           const uint32_t d = dst_base + r * 128 + ((c ^ (r & 7)) << 4);
@@ -161,6 +176,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const int STAGES = args.stages;
   const int STAGE_BYTES = gemm_stage_bytes(BN);
   const uint32_t IDESC = idesc_f16_f32acc(kGemmBM, (uint32_t)BN);
+  const int num_kb = args.num_k_blocks;
+  const int chunk_kb = args.chunk_kb;
+  const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -169,8 +187,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
   auto bar_empty = [&](int s) { return bar0 + 8u * (kGemmMaxStages + s); };
-  auto bar_tfull = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + a); };
-  auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + 2 + a); };
+  auto bar_cfull = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + a); };
+  auto bar_cempty = [&](int a) { return bar0 + 8u * (2 * kGemmMaxStages + 2 + a); };
   const uint32_t bar_drain = bar0 + 8u * (2 * kGemmMaxStages + 4);
   auto stage_a = [&](int s) { return sbase + (uint32_t)(s * STAGE_BYTES); };
   auto stage_b = [&](int s) { return sbase + (uint32_t)(s * STAGE_BYTES + L::A_BYTES); };
@@ -182,12 +200,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full(s), MODE == kLoadTma ? 1u : 128u);
+      mbar_init(bar_full(s), MODE == kLoadTma ? 1u : (uint32_t)kGemmCopyThreads);
       mbar_init(bar_empty(s), 1u);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(bar_tfull(a), 1u);
-      mbar_init(bar_tempty(a), (uint32_t)kGemmEpiWarps);
+      mbar_init(bar_cfull(a), 1u);
+      mbar_init(bar_cempty(a), (uint32_t)kGemmEpiWarps);
     }
     mbar_init(bar_drain, 1u);
     *abort_flag = 0;
@@ -206,8 +224,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-
-  const int num_kb = args.num_k_blocks;
 
   if (warp >= kGemmProdWarp0) {
     // ------------------------------------------------------------ producer
@@ -240,7 +256,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         }
       }
     } else {
-      const int pt = threadIdx.x - kGemmProdWarp0 * 32;  // 0..127
+      const int pt = threadIdx.x - kGemmProdWarp0 * 32;  // 0 .. kGemmCopyThreads-1
       // copies of a stage complete LAG iterations after they are issued;
       // LAG < STAGES (STAGES >= 4) keeps the ring from deadlocking
       constexpr int LAG = (MODE == kLoadCpAsync4) ? 3 : 0;
@@ -281,29 +297,33 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
-        if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, abort_flag)) break;
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kGemmMaxBN);
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
+        for (int c = 0; c < num_chunks && ok; ++c) {
+          if (!mbar_wait(bar_cempty(buf), buf_phase ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint64_t adesc = sdesc_kmajor_sw128(stage_a(stage));
-          const uint64_t bdesc = sdesc_kmajor_sw128(stage_b(stage));
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kGemmMaxBN);
+          const int kb_end = min(num_kb, (c + 1) * chunk_kb);
+          for (int kb = c * chunk_kb; kb < kb_end; ++kb) {
+            if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint64_t adesc = sdesc_kmajor_sw128(stage_a(stage));
+            const uint64_t bdesc = sdesc_kmajor_sw128(stage_b(stage));
+            const bool first = (kb == c * chunk_kb);
 #pragma unroll
-          for (int k = 0; k < kGemmBK / 16; ++k) {
-            // advance 16 elements = 32 bytes along K inside the swizzle row
-            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kGemmBK / 16; ++k) {
+              // advance 16 elements = 32 bytes along K inside the swizzle row
+              umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+            }
+            umma_commit(bar_empty(stage));  // frees the stage when these MMAs finish
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          umma_commit(bar_empty(stage));  // frees the stage when these MMAs finish
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          umma_commit(bar_cfull(buf));  // chunk sums ready for the epilogue
+          if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
         }
-        if (!ok) break;
-        umma_commit(bar_tfull(acc));  // accumulator ready for the epilogue
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       // every MMA this thread issued has finished before TMEM is released
       umma_commit(bar_drain);
@@ -312,91 +332,103 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp;  // TMEM lanes 32*ew .. 32*ew+31 = tile rows
-    __half* bias_s = reinterpret_cast<__half*>(smem + L::OFF_BIAS) + ew * kGemmMaxBN;
-    uint8_t* stg = smem + L::OFF_STG + ew * 2 * L::STG_BYTES;
-    const uint32_t stg_addr = sbase + L::OFF_STG + ew * 2 * L::STG_BYTES;
+    const int q = warp & 3;   // TMEM lane quadrant: tile rows 32q .. 32q+31
+    const int h = warp >> 2;  // column half
+    const int half0 = gemm_half0_cols(BN);
+    const int col0 = h == 0 ? 0 : half0;
+    const int ngroups = (h == 0 ? half0 : BN - half0) / 32;  // 32-column groups, 1..4
+    uint8_t* stg = smem + L::OFF_STG + warp * 2 * L::STG_BYTES;
+    const uint32_t stg_addr = sbase + L::OFF_STG + warp * 2 * L::STG_BYTES;
+    int sbuf = 0;
     int buf = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t buf_phase = 0;
     const int M = args.M, N = args.N;
-    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+    bool ok = true;
+    for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
       int mb, nb;
       gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       const int m0 = mb * kGemmBM, n0 = nb * BN;
-      // bias of this tile into warp-private shared memory, fetched before
-      // the accumulator wait so its latency overlaps the main loop
-      __syncwarp();
-      for (int j = lane; j < BN; j += 32) {
-        const int n = n0 + j;
-        bias_s[j] = (n < N) ? args.b[n] : __float2half_rn(0.0f);
+      float acc[kGemmHalfCols];
+#pragma unroll
+      for (int i = 0; i < kGemmHalfCols; ++i) acc[i] = 0.0f;
+      for (int c = 0; c < num_chunks; ++c) {
+        // warp-uniform decision: the TMEM loads below are warp-collective
+        const bool got = mbar_wait(bar_cfull(buf), buf_phase, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kGemmMaxBN + col0);
+#pragma unroll
+        for (int g = 0; g < kGemmHalfCols / 32; ++g) {
+          if (g < ngroups) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(g * 32), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)  // IEEE FP32 adds, round to nearest
+              add_f32x2(acc[g * 32 + j], acc[g * 32 + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cempty(buf));
+        if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
       }
-      __syncwarp();
-      // warp-uniform decision: the TMEM loads below are warp-collective
-      const bool got = mbar_wait(bar_tfull(acc), acc_phase, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after_sync();
-      const uint32_t trow = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kGemmMaxBN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(trow + (uint32_t)(c * 32), r);
-        tmem_ld_wait();
-        uint32_t packed[16];
-        const uint4* bv = reinterpret_cast<const uint4*>(bias_s + c * 32);
+      if (!ok) break;
+      // final epilogue of this tile from registers
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 bb = bv[q];
-          const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+      for (int g = 0; g < kGemmHalfCols / 32; ++g) {
+        if (g < ngroups) {
+          const int nc = n0 + col0 + g * 32;  // first column of this 32-column box
+          // bias of the box: lane l holds b[nc + l]; broadcast by shuffles
+          const __half bl = (nc + lane < N) ? args.b[nc + lane] : __float2half_rn(0.0f);
+          const unsigned short blu = __half_as_ushort(bl);
+          uint32_t packed[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = q * 4 + e;
+          for (int i = 0; i < 16; ++i) {
             // proj = RN16(acc) for two columns, then y = RN16(proj + b)
-            const __half2 p = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&bw[e]));
+            const __half2 p = __floats2half2_rn(acc[g * 32 + 2 * i], acc[g * 32 + 2 * i + 1]);
+            const uint32_t b2 = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
+                                ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
+            const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&b2));
             packed[i] = *reinterpret_cast<const uint32_t*>(&yv);
           }
-        }
-        if (args.tma_store) {
-          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
-          __syncwarp();
-        }
-        // row `lane` of the 32 x 32 box, 64-byte swizzle: chunk q at q ^ ((row >> 1) & 3)
-        uint8_t* rowp = stg + buf * L::STG_BYTES + lane * 64;
+          if (args.tma_store) {
+            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            __syncwarp();
+          }
+          // row `lane` of the 32 x 32 box, 64-byte swizzle: chunk j at j ^ ((row >> 1) & 3)
+          uint8_t* rowp = stg + sbuf * L::STG_BYTES + lane * 64;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int pos = q ^ ((lane >> 1) & 3);
-          *reinterpret_cast<uint4*>(rowp + pos * 16) =
-              make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-        }
-        if (args.tma_store) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_y, stg_addr + buf * L::STG_BYTES, n0 + c * 32, m0 + ew * 32);
-            bulk_commit_group();
+          for (int j = 0; j < 4; ++j) {
+            const int pos = j ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4*>(rowp + pos * 16) =
+                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
           }
-        } else {
-          __syncwarp();
-          const uint8_t* box = stg + buf * L::STG_BYTES;
-          const int col = n0 + c * 32 + lane;
-#pragma unroll 4
-          for (int rr = 0; rr < 32; ++rr) {
-            const int row = m0 + ew * 32 + rr;
-            if (row < M && col < N) {
-              const int pos = (lane >> 3) ^ ((rr >> 1) & 3);
-              args.y[(size_t)row * N + col] =
-                  *reinterpret_cast<const __half*>(box + rr * 64 + pos * 16 + (lane & 7) * 2);
+          if (args.tma_store) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc, m0 + q * 32);
+              bulk_commit_group();
             }
+          } else {
+            __syncwarp();
+            const uint8_t* box = stg + sbuf * L::STG_BYTES;
+            const int col = nc + lane;
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr) {
+              const int row = m0 + q * 32 + rr;
+              if (row < M && col < N) {
+                const int pos = (lane >> 3) ^ ((rr >> 1) & 3);
+                args.y[(size_t)row * N + col] =
+                    *reinterpret_cast<const __half*>(box + rr * 64 + pos * 16 + (lane & 7) * 2);
+              }
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          sbuf ^= 1;
         }
-        buf ^= 1;
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty(acc));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (args.tma_store && lane == 0) bulk_wait_group<0>();
     __syncwarp();

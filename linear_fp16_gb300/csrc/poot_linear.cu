@@ -21,6 +21,12 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr int kMaxDevices = 64;
 
 using Layout = GemmLayout;
+// K elements per TMEM accumulation chain before the FP32 register promotion.
+// Measured on GB300 (8192x14336x4096, 1.38 M sampled outputs): chunks of
+// 1024 leave 4 outputs beyond 2 FP16 ulps of a sequential FP32 sum (IEEE
+// reorderings leave 2, one chain over all of K leaves 28) for about 1-2%
+// of run time; 512 costs 2-3% more for no further gain.
+constexpr int kDefaultChunkK = 1024;
 
 constexpr int kGemvSmemBudget = 64 * 1024;  // bytes of x staged per GEMV block
 
@@ -169,7 +175,7 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 }
 
 struct GemmPlan {
-  int bn, stages, group_m;
+  int bn, stages, group_m, chunk_kb;
 };
 
 // Tile plan from a cost model: each CTA runs ceil(tiles / SMs) tiles; a
@@ -179,7 +185,7 @@ struct GemmPlan {
 // 128 B/cycle.  The efficiencies of narrower tiles (more x re-reads, more
 // epilogue work per FLOP) were measured on GB300 for 224 (0.90 - 0.97) and
 // extrapolated below it.  Ties go to the wider tile.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int group_req) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int group_req, int chunk_req) {
   const int64_t num_m = (M + kGemmBM - 1) / kGemmBM;
   const int64_t num_kb = (K + kGemmBK - 1) / kGemmBK;
   int best_bn = 256;
@@ -202,12 +208,16 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int gro
   // tiles are walked in groups of 8 M blocks (1024 rows of x); measured on
   // GB300 to beat groups of 16, 32 and 64 on 4096^3 and 8192x14336x4096
   p.group_m = group_req > 0 ? group_req : 8;
+  // K elements summed in TMEM before the FP32 register promotion
+  const int chunk_k = chunk_req > 0 ? chunk_req : kDefaultChunkK;
+  p.chunk_kb = chunk_k / kGemmBK;
   return p;
 }
 
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
-                int64_t M, int64_t N, int64_t K, int bn_req, int group_req, cudaStream_t stream) {
-  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, bn_req, group_req);
+                int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req,
+                cudaStream_t stream) {
+  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, bn_req, group_req, chunk_req);
   GemmArgs a;
   a.x = static_cast<const __half*>(x);
   a.w = static_cast<const __half*>(w);
@@ -219,6 +229,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   a.bn = plan.bn;
   a.stages = plan.stages;
   a.group_m = plan.group_m;
+  a.chunk_kb = plan.chunk_kb;
   a.num_m_blocks = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
   a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
   a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
@@ -330,6 +341,7 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
   if (o.gemm_tile_n != 0 && (o.gemm_tile_n < 64 || o.gemm_tile_n > kGemmMaxBN || o.gemm_tile_n % 32 != 0))
     return POOT_ERR_INVALID_ARG;
   if (o.gemm_group_m < 0) return POOT_ERR_INVALID_ARG;
+  if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return POOT_ERR_INVALID_ARG;
   if (variant == POOT_VARIANT_AUTO) {
     variant = choose_variant(x, w, M, N, K);
   } else if (!variant_applicable(variant, x, w, M, N, K)) {
@@ -357,7 +369,8 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
     case POOT_VARIANT_GEMV_SCALAR:
       return launch_gemv(variant, *st, x, w, b, y, M, N, K, gemv_wpr, stream);
     default:
-      return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, stream);
+      return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
+                         stream);
   }
 }
 

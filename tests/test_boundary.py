@@ -133,6 +133,12 @@ def test_bad_gemm_tile_width(tile_n):
         L.POOT_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("chunk", [-64, 32, 100])
+def test_bad_gemm_k_chunk(chunk):
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_k_chunk=chunk), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
 def test_bad_gemm_group():
     assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_group_m=-1), 0) == \
         L.POOT_ERR_INVALID_ARG
