@@ -16,7 +16,7 @@
 //   warps 9+   producer: TMA tiles of x [128 x 64] and W [BN x 64], both
 //              K-major with the 128-byte swizzle, into a ring of stages; or,
 //              for row pitches TMA cannot address (K % 8 != 0 or unaligned
-//              pointers), two warps that copy the same swizzled layout with
+//              pointers), three warps that copy the same swizzled layout with
 //              4-byte cp.async or 2-byte register copies.
 // Tails in M, N and K: TMA zero-fills out-of-range reads (zeros add nothing
 // to the sum) and clips stores; the copy producers zero-fill by predicate.
@@ -59,11 +59,11 @@ constexpr int kGemmMaxStages = 8;
 constexpr int kGemmEpiWarps = 8;
 constexpr int kGemmMmaWarp = 8;
 constexpr int kGemmProdWarp0 = 9;
-constexpr int kGemmCopyThreads = 64;                 // copy producers: two warps
+constexpr int kGemmCopyThreads = 96;                 // copy producers: three warps
 constexpr uint32_t kGemmTmemCols = 2 * kGemmMaxBN;  // two chunk buffers, 256 columns apart
 constexpr int kGemmHalfCols = kGemmMaxBN / 2;        // columns per epilogue warp (max)
 
-__host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 2; }
+__host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 3; }
 __host__ __device__ constexpr int gemm_threads(int mode) {
   return (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
 }
@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // prologue done; global memory is touched only after the previous grid
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp >= kGemmProdWarp0) {
     // ------------------------------------------------------------ producer

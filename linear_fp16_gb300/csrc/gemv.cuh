@@ -47,6 +47,8 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 // (K % 8 == 0 and both 16-byte aligned); otherwise 2-byte loads.
 template <int MT, bool VEC>
 __global__ void __launch_bounds__(kGemvThreads) gemv_f16_kernel(const GemvArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ uint4 gemv_smem[];
   __half* xs = reinterpret_cast<__half*>(gemv_smem);  // [MT][kc]
   __shared__ float red[kGemvWarps][MT];
@@ -166,6 +168,7 @@ constexpr int kGemvRowVpl = 16;  // vectors per lane per chunk (16 * 32 * 8 = 40
 
 template <int MT>
 __global__ void __launch_bounds__(kGemvRowThreads) gemv_f16_rows_kernel(const GemvArgs a) {
+  grid_dep_wait();
   __shared__ float red[kGemvRowWarps][MT];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -225,6 +228,9 @@ __global__ void __launch_bounds__(kGemvRowThreads) gemv_f16_rows_kernel(const Ge
     }
   }
 
+  // the W stream is done: let the next kernel in the stream start launching
+  // (earlier, its blocks would compete with this grid's for SM slots)
+  grid_dep_launch();
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
 #pragma unroll
@@ -281,6 +287,8 @@ __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, ui
 // NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16)
 template <int NT>
 __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const GemvArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float red[kGemvMmaWarps][32][4 * NT];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -306,7 +314,7 @@ __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const Gem
   for (int q = 0; q < NT; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
   const uint4 zero = make_uint4(0, 0, 0, 0);
 
-  constexpr int U = 4;  // steps of 32 along K per batch
+  constexpr int U = NT == 1 ? 8 : 4;  // steps of 32 along K per batch
   for (int k0 = k_begin; k0 < k_end; k0 += 32 * U) {
     uint4 va[U], vb[U], vx[U][NT];
 #pragma unroll
@@ -354,6 +362,8 @@ __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const Gem
 // K == 0: the sum is +0, so y[m, n] = RN16(+0 + b[n]) (a -0 bias gives +0).
 __global__ void bias_only_kernel(const __half* __restrict__ b, __half* __restrict__ y, long long M,
                                  long long N) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long total = M * N;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {

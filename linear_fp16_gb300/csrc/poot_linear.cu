@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "poot_linear.h"
 #include "gemm_tcgen05.cuh"
@@ -107,6 +108,27 @@ int device_state(int* dev_out, DeviceState** st_out) {
   *dev_out = dev;
   *st_out = &st;
   return st.status;
+}
+
+// Launch with programmatic stream serialisation (see grid_dep_wait in
+// ptx.cuh): the kernel may be scheduled while the previous kernel in the
+// stream drains; it waits for that kernel before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  std::memset(attr, 0, sizeof(attr));
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -251,30 +273,33 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     return cuda_fail(cudaErrorInvalidValue);
 
   const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
+  cudaError_t e;
   switch (variant) {
     case POOT_VARIANT_GEMM_TMA:
-      gemm_f16_tcgen05_kernel<kLoadTma><<<grid, gemm_threads(kLoadTma), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      e = launch(gemm_f16_tcgen05_kernel<kLoadTma>, dim3(grid), dim3(gemm_threads(kLoadTma)), Layout::DYN_BYTES,
+                 stream, tx, tw, ty, a);
       break;
     case POOT_VARIANT_GEMM_CPASYNC:
-      gemm_f16_tcgen05_kernel<kLoadCpAsync4>
-          <<<grid, gemm_threads(kLoadCpAsync4), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4>, dim3(grid), dim3(gemm_threads(kLoadCpAsync4)),
+                 Layout::DYN_BYTES, stream, tx, tw, ty, a);
       break;
     default:
-      gemm_f16_tcgen05_kernel<kLoadReg16><<<grid, gemm_threads(kLoadReg16), Layout::DYN_BYTES, stream>>>(tx, tw, ty, a);
+      e = launch(gemm_f16_tcgen05_kernel<kLoadReg16>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
+                 Layout::DYN_BYTES, stream, tx, tw, ty, a);
       break;
   }
-  const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
 
 template <bool VEC>
-void launch_gemv_mt(int mt, dim3 grid, size_t smem, cudaStream_t stream, const GemvArgs& a) {
+cudaError_t launch_gemv_mt(int mt, dim3 grid, size_t smem, cudaStream_t stream, const GemvArgs& a) {
+  const dim3 block(kGemvThreads);
   switch (mt) {
-    case 1: gemv_f16_kernel<1, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
-    case 2: gemv_f16_kernel<2, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
-    case 4: gemv_f16_kernel<4, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
-    case 8: gemv_f16_kernel<8, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
-    default: gemv_f16_kernel<16, VEC><<<grid, kGemvThreads, smem, stream>>>(a); break;
+    case 1: return launch(gemv_f16_kernel<1, VEC>, grid, block, smem, stream, a);
+    case 2: return launch(gemv_f16_kernel<2, VEC>, grid, block, smem, stream, a);
+    case 4: return launch(gemv_f16_kernel<4, VEC>, grid, block, smem, stream, a);
+    case 8: return launch(gemv_f16_kernel<8, VEC>, grid, block, smem, stream, a);
+    default: return launch(gemv_f16_kernel<16, VEC>, grid, block, smem, stream, a);
   }
 }
 
@@ -307,25 +332,26 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
   if (blocks > INT32_MAX) return POOT_ERR_INVALID_ARG;
   const size_t smem = static_cast<size_t>(mt) * static_cast<size_t>(kc) * 2;
+  cudaError_t e;
   if (variant == POOT_VARIANT_GEMV && mt <= 2 && wpr <= kGemvRowWarps) {
     const int rpb = kGemvRowWarps / wpr;
-    const unsigned rblocks = static_cast<unsigned>((N + rpb - 1) / rpb);
+    const dim3 rgrid(static_cast<unsigned>((N + rpb - 1) / rpb));
     if (mt == 1)
-      gemv_f16_rows_kernel<1><<<rblocks, kGemvRowThreads, 0, stream>>>(a);
+      e = launch(gemv_f16_rows_kernel<1>, rgrid, dim3(kGemvRowThreads), 0, stream, a);
     else
-      gemv_f16_rows_kernel<2><<<rblocks, kGemvRowThreads, 0, stream>>>(a);
+      e = launch(gemv_f16_rows_kernel<2>, rgrid, dim3(kGemvRowThreads), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV && wpr_req == 0) {
     // 3 <= M <= 16 on the tensor cores, 16 rows of W per block
-    const unsigned mblocks = static_cast<unsigned>((N + 15) / 16);
+    const dim3 mgrid(static_cast<unsigned>((N + 15) / 16));
     if (M <= 8)
-      gemv_f16_mma_kernel<1><<<mblocks, kGemvMmaThreads, 0, stream>>>(a);
+      e = launch(gemv_f16_mma_kernel<1>, mgrid, dim3(kGemvMmaThreads), 0, stream, a);
     else
-      gemv_f16_mma_kernel<2><<<mblocks, kGemvMmaThreads, 0, stream>>>(a);
-  } else if (variant == POOT_VARIANT_GEMV)
-    launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
-  else
-    launch_gemv_mt<false>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
-  const cudaError_t e = cudaGetLastError();
+      e = launch(gemv_f16_mma_kernel<2>, mgrid, dim3(kGemvMmaThreads), 0, stream, a);
+  } else if (variant == POOT_VARIANT_GEMV) {
+    e = launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
+  } else {
+    e = launch_gemv_mt<false>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
+  }
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
 
@@ -360,9 +386,9 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
       int64_t blocks = (total + 255) / 256;
       const int64_t cap = int64_t(st->sm_count) * 8;
       if (blocks > cap) blocks = cap;
-      bias_only_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-          static_cast<const __half*>(b), static_cast<__half*>(y), M, N);
-      const cudaError_t e = cudaGetLastError();
+      const cudaError_t e = launch(bias_only_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                                   static_cast<const __half*>(b), static_cast<__half*>(y), (long long)M,
+                                   (long long)N);
       return e == cudaSuccess ? POOT_OK : cuda_fail(e);
     }
     case POOT_VARIANT_GEMV:

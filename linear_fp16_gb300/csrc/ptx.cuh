@@ -28,6 +28,16 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// Kernels are launched with programmatic stream serialisation, so a kernel
+// may start while the previous kernel in the stream is still finishing.
+// grid_dep_wait() blocks until every earlier grid has completed and its
+// memory is visible; each kernel calls it before its first global-memory
+// access, so the overlap is limited to launch and prologue work.
+// grid_dep_launch() lets the next kernel start launching early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
