@@ -167,8 +167,7 @@ constexpr int kGemvRowThreads = kGemvRowWarps * 32;
 constexpr int kGemvRowVpl = 16;  // vectors per lane per chunk (16 * 32 * 8 = 4096 elements)
 
 template <int MT>
-__global__ void __launch_bounds__(kGemvRowThreads) gemv_f16_rows_kernel(const GemvArgs a) {
-  grid_dep_wait();
+__global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const GemvArgs a) {
   __shared__ float red[kGemvRowWarps][MT];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -184,6 +183,7 @@ __global__ void __launch_bounds__(kGemvRowThreads) gemv_f16_rows_kernel(const Ge
   const int v_end = min(nvec, (part + 1) * seg_per_part * 32);
   const uint4* __restrict__ wv = reinterpret_cast<const uint4*>(a.w + (size_t)(active ? row : 0) * a.K);
   const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(a.x);
+  grid_dep_wait();
 
   float acc[MT];
 #pragma unroll
@@ -287,8 +287,6 @@ __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, ui
 // NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16)
 template <int NT>
 __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const GemvArgs a) {
-  grid_dep_wait();
-  grid_dep_launch();
   __shared__ float red[kGemvMmaWarps][32][4 * NT];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -305,6 +303,14 @@ __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const Gem
   const __half* __restrict__ x0 = a.x + (size_t)(g < M ? g : 0) * K;
   const __half* __restrict__ x1 = a.x + (size_t)(g + 8 < M ? g + 8 : 0) * K;
   const bool okA = nA < N, okB = nB < N, okx0 = g < M, okx1 = (NT > 1) && (g + 8 < M);
+  // start this warp's K slice of its 16 W rows towards L2 while the
+  // previous grid drains (lane 4g prefetches rows nA and nB)
+  if (t == 0 && k_end > k_begin) {
+    if (okA) prefetch_l2_bulk(wa + k_begin, (uint32_t)(k_end - k_begin) * 2u);
+    if (okB) prefetch_l2_bulk(wb + k_begin, (uint32_t)(k_end - k_begin) * 2u);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
   // bias of this lane's two output features, fetched early
   const float bA = (warp == 0 && okA) ? __half2float(a.b[nA]) : 0.0f;
   const float bB = (warp == 0 && okB) ? __half2float(a.b[nB]) : 0.0f;

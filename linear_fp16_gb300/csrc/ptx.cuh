@@ -136,6 +136,14 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, size a multiple
+// of 16).  Returns no data, so it may run before grid_dep_wait(): L2 is the
+// point of coherence for every SM, and a later write by an earlier grid
+// still lands there before this grid's loads read it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- LDGSTS (non-bulk cp.async) ----------------------------------------------
 // Copies `src_bytes` (0 or 4) bytes and zero-fills the rest of the 4 bytes.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
