@@ -124,6 +124,11 @@ typedef struct poot_linear_options {
                                 before the partial sums are added, in IEEE
                                 FP32, into the running sum.  A value >= K
                                 keeps the whole sum on the tensor core */
+    int gemm_cluster;        /* 0 = automatic; 1 = one CTA per 128-row tile;
+                                2 = CTA pairs sharing each W tile on 256-row
+                                tiles (2-SM MMA); 4 = two such pairs on
+                                neighbouring N tiles sharing the x tile.
+                                2 and 4 need the GEMM_TMA variant */
 } poot_linear_options;
 
 /*

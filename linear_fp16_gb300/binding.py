@@ -43,12 +43,12 @@ class Options(ctypes.Structure):
     """struct poot_linear_options (include/poot_linear.h)."""
     _fields_ = [("variant", ctypes.c_int), ("gemv_warps_per_row", ctypes.c_int),
                 ("gemm_tile_n", ctypes.c_int), ("gemm_group_m", ctypes.c_int),
-                ("gemm_k_chunk", ctypes.c_int)]
+                ("gemm_k_chunk", ctypes.c_int), ("gemm_cluster", ctypes.c_int)]
 
 
 def options(variant: int = -1, gemv_warps_per_row: int = 0, gemm_tile_n: int = 0,
-            gemm_group_m: int = 0, gemm_k_chunk: int = 0) -> Options:
-    return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m, gemm_k_chunk)
+            gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0) -> Options:
+    return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster)
 
 
 # (name, restype, argtypes) of every exported symbol
@@ -153,7 +153,8 @@ def _check(t, name, ndim):
 
 
 def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row: int = 0,
-           gemm_tile_n: int = 0, gemm_group_m: int = 0, gemm_k_chunk: int = 0, stream=None):
+           gemm_tile_n: int = 0, gemm_group_m: int = 0, gemm_k_chunk: int = 0,
+           gemm_cluster: int = 0, stream=None):
     """y = FP16(x . W^T) + b with x [M,K], w [N,K], b [N] fp16 CUDA tensors.
 
     Runs on ``stream`` (default: the current torch stream of x's device) and
@@ -181,7 +182,7 @@ def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row
         s = torch.cuda.current_stream(dev) if stream is None else stream
         rc = poot_linear_f16_ex(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
                                 options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m,
-                                        gemm_k_chunk),
+                                        gemm_k_chunk, gemm_cluster),
                                 s.cuda_stream)
     if rc != POOT_OK:
         raise PootLinearError(rc, "poot_linear_f16")

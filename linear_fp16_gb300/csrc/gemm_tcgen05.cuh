@@ -86,11 +86,16 @@ struct GemmLayout {
   static_assert(DYN_BYTES <= 232448, "more shared memory than a CTA can have");
 };
 
-__host__ __device__ constexpr int gemm_b_bytes(int bn) { return bn * kGemmBK * 2; }
-__host__ __device__ constexpr int gemm_stage_bytes(int bn) { return GemmLayout::A_BYTES + gemm_b_bytes(bn); }
-__host__ __device__ constexpr int gemm_max_stages(int bn) {
-  return GemmLayout::RING_BYTES / gemm_stage_bytes(bn) < kGemmMaxStages
-             ? GemmLayout::RING_BYTES / gemm_stage_bytes(bn) : kGemmMaxStages;
+// W rows a CTA loads per stage: the whole tile width, or half of it when a
+// CTA pair shares the W tile (2-SM MMA).
+__host__ __device__ constexpr int gemm_b_rows(int bn, bool pair) { return pair ? bn / 2 : bn; }
+__host__ __device__ constexpr int gemm_b_bytes(int bn, bool pair = false) { return gemm_b_rows(bn, pair) * kGemmBK * 2; }
+__host__ __device__ constexpr int gemm_stage_bytes(int bn, bool pair = false) {
+  return GemmLayout::A_BYTES + gemm_b_bytes(bn, pair);
+}
+__host__ __device__ constexpr int gemm_max_stages(int bn, bool pair = false) {
+  return GemmLayout::RING_BYTES / gemm_stage_bytes(bn, pair) < kGemmMaxStages
+             ? GemmLayout::RING_BYTES / gemm_stage_bytes(bn, pair) : kGemmMaxStages;
 }
 // Columns of the first epilogue half (a multiple of 32); the second half
 // takes the rest.
@@ -166,16 +171,41 @@ __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* 
   }
 }
 
-template <int MODE>
+// CL = cluster size.  CL = 1: one CTA per 128 x BN tile.
+// CL = 2: 2-SM MMA.  Two CTAs of a cluster (a pair: ranks 0 and 1) compute
+// one 256 x BN output tile: each loads its 128 rows of x and BN/2 rows of W
+// into its own shared memory, the even CTA issues tcgen05.mma.cta_group::2
+// for both (each CTA's TMEM receives its 128 rows), and commits arrive in
+// both CTAs.  The odd CTA's TMA loads complete on the even CTA's "full"
+// barriers, and both CTAs' epilogue warps release chunk buffers on the even
+// CTA's "cempty" barriers.  Per SM a stage holds 32 KB instead of 48 KB
+// (BN = 256), so the ring is six stages deep, and W is read once per pair.
+// CL = 4: two pairs on adjacent N tiles of the same 256 rows.  CTAs r and
+// r ^ 2 need the same x rows: each loads half of them and multicasts it to
+// both, so a CTA reads 24 KB per stage from L2 instead of 32 KB.  A stage is
+// refilled only after both pairs' MMAs released it (each "empty" barrier
+// counts one multicast commit from each pair).
+template <int MODE, int CL>
 __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     gemm_f16_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x,
                             const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_y, const GemmArgs args) {
+  constexpr bool PAIR = CL >= 2;
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
+  static_assert(!PAIR || MODE == kLoadTma, "the CTA-pair kernel loads through TMA only");
   using L = GemmLayout;
   const int BN = args.bn;
   const int STAGES = args.stages;
-  const int STAGE_BYTES = gemm_stage_bytes(BN);
-  const uint32_t IDESC = idesc_f16_f32acc(kGemmBM, (uint32_t)BN);
+  const int STAGE_BYTES = gemm_stage_bytes(BN, PAIR);
+  const uint32_t IDESC = idesc_f16_f32acc(PAIR ? 2 * kGemmBM : kGemmBM, (uint32_t)BN);
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank & 1u;               // row half of the pair's tile
+  const uint32_t pair_id = crank >> 1;            // CL = 4: which of the two N tiles
+  const uint32_t lead_rank = crank & ~1u;         // even CTA of this pair
+  const bool leader = (rank == 0);
+  const int unit = (int)(blockIdx.x / CL);        // cluster (or CTA) index
+  const int units = (int)(gridDim.x / CL);
+  const int tile_rows = PAIR ? 2 * kGemmBM : kGemmBM;
   const int num_kb = args.num_k_blocks;
   const int chunk_kb = args.chunk_kb;
   const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
@@ -201,19 +231,24 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), MODE == kLoadTma ? 1u : (uint32_t)kGemmCopyThreads);
-      mbar_init(bar_empty(s), 1u);
+      mbar_init(bar_empty(s), CL == 4 ? 2u : 1u);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_cfull(a), 1u);
-      mbar_init(bar_cempty(a), (uint32_t)kGemmEpiWarps);
+      mbar_init(bar_cempty(a), (uint32_t)(PAIR ? 2 * kGemmEpiWarps : kGemmEpiWarps));
     }
     mbar_init(bar_drain, 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kGemmMmaWarp) {
-    tmem_alloc(smem_addr(tmem_slot), kGemmTmemCols);
-    tmem_relinquish_alloc_permit();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_addr(tmem_slot), kGemmTmemCols);
+      tmem_relinquish_alloc_permit_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), kGemmTmemCols);
+      tmem_relinquish_alloc_permit();
+    }
   }
   if (MODE == kLoadTma && warp == kGemmProdWarp0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
@@ -222,6 +257,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   if (warp == 0 && lane == 0 && args.tma_store) tma_prefetch_desc(&tm_y);
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote signal
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // prologue done; global memory is touched only after the previous grid
@@ -236,26 +272,47 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        for (int t = unit; t < args.num_tiles && ok; t += units) {
           int mb, nb;
           gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+          if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;  // this pair's N tile
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t fb = bar_full(stage);
-            mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-            tma_load_2d(stage_a(stage), &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
-            tma_load_2d(stage_b(stage), &tm_w, fb, kb * kGemmBK, nb * BN);
+            if constexpr (PAIR) {
+              // both CTAs' bytes complete on the even CTA's barrier
+              const uint32_t fb0 = map_to_cta(fb, lead_rank);
+              if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
+              const int arow = mb * tile_rows + (int)rank * kGemmBM;
+              if constexpr (CL == 4) {
+                // half of the x tile, into this CTA and its counterpart in the other pair
+                const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
+                tma_load_2d_pair_multicast(stage_a(stage) + pair_id * (kGemmBM / 2) * 128u, &tm_x, fb0, kb * kGemmBK,
+                                           arow + (int)pair_id * (kGemmBM / 2), mask);
+              } else {
+                tma_load_2d_pair(stage_a(stage), &tm_x, fb0, kb * kGemmBK, arow);
+              }
+              tma_load_2d_pair(stage_b(stage), &tm_w, fb0, kb * kGemmBK, nb * BN + (int)rank * (BN / 2));
+            } else {
+              mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+              tma_load_2d(stage_a(stage), &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
+              tma_load_2d(stage_b(stage), &tm_w, fb, kb * kGemmBK, nb * BN);
+            }
             ++issued;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
         // Let the last loads land before the CTA can exit (their barrier
-        // phases complete on their own; nothing else arrives there).
-        int s = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < STAGES && i < issued; ++i) {
-          if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
-          mbar_wait(bar_full(s), ph, nullptr);
+        // phases complete on their own; nothing else arrives there).  In a
+        // pair the even CTA's barriers also count the odd CTA's bytes; the
+        // odd CTA is held by the closing cluster barrier instead.
+        if (leader) {
+          int s = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < STAGES && i < issued; ++i) {
+            if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+            mbar_wait(bar_full(s), ph, nullptr);
+          }
         }
       }
     } else {
@@ -265,7 +322,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       constexpr int LAG = (MODE == kLoadCpAsync4) ? 3 : 0;
       long long it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < args.num_tiles && ok; t += units) {
         int mb, nb;
         gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -297,13 +354,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     }
   } else if (warp == kGemmMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t buf_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < args.num_tiles && ok; t += units) {
         for (int c = 0; c < num_chunks && ok; ++c) {
           if (!mbar_wait(bar_cempty(buf), buf_phase ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after_sync();
@@ -318,18 +375,28 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 #pragma unroll
             for (int k = 0; k < kGemmBK / 16; ++k) {
               // advance 16 elements = 32 bytes along K inside the swizzle row
-              umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+              if constexpr (PAIR)
+                umma_f16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+              else
+                umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
             }
-            umma_commit(bar_empty(stage));  // frees the stage when these MMAs finish
+            // frees the stage (in both CTAs of a pair) when these MMAs finish
+            // (with CL = 4 in all four CTAs: a stage is refilled by both pairs)
+            if constexpr (CL == 4) umma_commit_pair(bar_empty(stage), 0xF);
+            else if constexpr (PAIR) umma_commit_pair(bar_empty(stage), 3);
+            else umma_commit(bar_empty(stage));
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          umma_commit(bar_cfull(buf));  // chunk sums ready for the epilogue
+          // chunk sums ready for the epilogue(s)
+          if constexpr (PAIR) umma_commit_pair(bar_cfull(buf), (uint16_t)(3u << lead_rank));
+          else umma_commit(bar_cfull(buf));
           if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
         }
       }
       // every MMA this thread issued has finished before TMEM is released
-      umma_commit(bar_drain);
+      if constexpr (PAIR) umma_commit_pair(bar_drain, (uint16_t)(1u << lead_rank));
+      else umma_commit(bar_drain);
       mbar_wait(bar_drain, 0u, nullptr);
     }
     __syncwarp();
@@ -347,10 +414,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     uint32_t buf_phase = 0;
     const int M = args.M, N = args.N;
     bool ok = true;
-    for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+    for (int t = unit; t < args.num_tiles && ok; t += units) {
       int mb, nb;
       gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
-      const int m0 = mb * kGemmBM, n0 = nb * BN;
+      if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;
+      const int m0 = mb * tile_rows + (int)rank * kGemmBM, n0 = nb * BN;
       float acc[kGemmHalfCols];
 #pragma unroll
       for (int i = 0; i < kGemmHalfCols; ++i) acc[i] = 0.0f;
@@ -373,7 +441,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_cempty(buf));
+        if (lane == 0) {
+          if constexpr (PAIR) mbar_arrive_cluster(map_to_cta(bar_cempty(buf), lead_rank));
+          else mbar_arrive(bar_cempty(buf));
+        }
         if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
       }
       if (!ok) break;
@@ -439,9 +510,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  // a pair's CTAs stay until the even CTA's MMAs (reading both CTAs' shared
+  // memory and writing both TMEMs) and every remote arrive are done
+  if constexpr (PAIR) cluster_sync();
   if (warp == kGemmMmaWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kGemmTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kGemmTmemCols);
+    else tmem_dealloc(tmem_base, kGemmTmemCols);
   }
 }
 

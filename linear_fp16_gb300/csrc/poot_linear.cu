@@ -37,6 +37,7 @@ struct DeviceState {
   bool ready = false;
   int status = POOT_OK;  // POOT_OK or POOT_ERR_UNSUPPORTED_DEVICE / CUDA
   int sm_count = 0;
+  int max_clusters4 = 0;  // co-resident 4-CTA clusters of the GEMM kernel
 };
 
 std::mutex g_mu;
@@ -49,10 +50,29 @@ int cuda_fail(cudaError_t e) {
   return POOT_ERR_CUDA;
 }
 
-template <int MODE>
+template <int MODE, int CL>
 cudaError_t set_gemm_attrs() {
-  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout::DYN_BYTES);
+}
+
+// How many 4-CTA clusters of the GEMM fit on the device at once (clusters
+// live inside one GPC, so this can be less than SMs / 4).
+cudaError_t query_max_clusters4(int* out) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(4);
+  cfg.blockDim = dim3(gemm_threads(kLoadTma));
+  cfg.dynamicSmemBytes = Layout::DYN_BYTES;
+  cudaLaunchAttribute attr[1];
+  std::memset(attr, 0, sizeof(attr));
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, gemm_f16_tcgen05_kernel<kLoadTma, 4>, &cfg);
 }
 
 template <int MT, bool VEC>
@@ -88,9 +108,10 @@ int device_state(int* dev_out, DeviceState** st_out) {
         if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
         g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
       }
-      if ((e = set_gemm_attrs<kLoadTma>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadCpAsync4>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadReg16>()) != cudaSuccess ||
+      if ((e = set_gemm_attrs<kLoadTma, 1>()) != cudaSuccess || (e = set_gemm_attrs<kLoadTma, 2>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 4>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadCpAsync4, 1>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadReg16, 1>()) != cudaSuccess ||
           (e = set_gemv_attrs<1, true>()) != cudaSuccess || (e = set_gemv_attrs<2, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<4, true>()) != cudaSuccess || (e = set_gemv_attrs<8, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<16, true>()) != cudaSuccess ||
@@ -100,6 +121,9 @@ int device_state(int* dev_out, DeviceState** st_out) {
           (e = set_gemv_attrs<8, false>()) != cudaSuccess ||
           (e = set_gemv_attrs<16, false>()) != cudaSuccess)
         return cuda_fail(e);
+      int mc4 = 0;
+      if ((e = query_max_clusters4(&mc4)) != cudaSuccess) return cuda_fail(e);
+      st.max_clusters4 = mc4;
       st.sm_count = sms;
       st.status = POOT_OK;
       st.ready = true;
@@ -113,22 +137,36 @@ int device_state(int* dev_out, DeviceState** st_out) {
 // Launch with programmatic stream serialisation (see grid_dep_wait in
 // ptx.cuh): the kernel may be scheduled while the previous kernel in the
 // stream drains; it waits for that kernel before touching global memory.
+// cluster_x > 1 launches clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                   Args&&... args) {
+cudaError_t launch_clustered(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             unsigned cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   std::memset(attr, 0, sizeof(attr));
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args&&... args) {
+  return launch_clustered(kernel, grid, block, smem, stream, 1u, std::forward<Args>(args)...);
 }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -198,6 +236,8 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 struct GemmPlan {
   int bn, stages, group_m, chunk_kb;
+  int cluster;  // 1: single CTAs; 2: CTA pairs (2-SM MMA); 4: two pairs sharing x
+  bool pair;    // cluster >= 2 (256-row tiles)
 };
 
 // Tile plan from a cost model: each CTA runs ceil(tiles / SMs) tiles; a
@@ -207,8 +247,22 @@ struct GemmPlan {
 // 128 B/cycle.  The efficiencies of narrower tiles (more x re-reads, more
 // epilogue work per FLOP) were measured on GB300 for 224 (0.90 - 0.97) and
 // extrapolated below it.  Ties go to the wider tile.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int group_req, int chunk_req) {
-  const int64_t num_m = (M + kGemmBM - 1) / kGemmBM;
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, int bn_req, int group_req,
+                   int chunk_req, int cluster_req, bool tma) {
+  // CTA pairs (2-SM MMA) for large problems; single CTAs when M is small (a
+  // pair's 256-row tile would be mostly empty) or the operands need copies.
+  // Clusters of two pairs sharing the x tile cut L2 reads by a fifth but fit
+  // only 36 clusters (144 SMs); interleaved timing on GB300 showed no gain
+  // over pairs on 4096^3 and 8192x14336x4096, so they are opt-in.
+  int cluster = 1;
+  if (tma) {
+    if (cluster_req != 0) cluster = cluster_req;
+    else if (M >= 512 && N >= 512) cluster = 2;
+  }
+  const bool pair = cluster >= 2;
+  const int64_t bm = pair ? 2 * kGemmBM : kGemmBM;
+  const int64_t slots = cluster == 4 ? 2 * int64_t(max_clusters4) : pair ? sms / 2 : sms;
+  const int64_t num_m = (M + bm - 1) / bm;
   const int64_t num_kb = (K + kGemmBK - 1) / kGemmBK;
   int best_bn = 256;
   int64_t best = INT64_MAX;
@@ -218,18 +272,21 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int gro
     const int bn = cands[i];
     if (bn_req != 0 && bn != bn_req) continue;
     const int64_t tiles = num_m * ((N + bn - 1) / bn);
-    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t waves = (tiles + slots - 1) / slots;
     const int64_t per_kb = (2 * bn > 128 + bn) ? 2 * bn : 128 + bn;
     const int64_t cost = waves * (num_kb * per_kb * 100 / eff_pct[i] + 2000);
     if (cost < best) { best = cost; best_bn = bn; }
   }
   if (bn_req != 0) best_bn = bn_req;
   GemmPlan p;
+  p.cluster = cluster;
+  p.pair = pair;
   p.bn = best_bn;
-  p.stages = gemm_max_stages(best_bn);
-  // tiles are walked in groups of 8 M blocks (1024 rows of x); measured on
-  // GB300 to beat groups of 16, 32 and 64 on 4096^3 and 8192x14336x4096
-  p.group_m = group_req > 0 ? group_req : 8;
+  p.stages = gemm_max_stages(best_bn, pair);
+  // tiles are walked in groups of 1024 rows of x (8 single-CTA M blocks, 4
+  // pair M blocks); measured on GB300 to beat 512, 1536, 2048, 4096 and all
+  // rows on 4096^3 and 8192x14336x4096
+  p.group_m = group_req > 0 ? group_req : (pair ? 4 : 8);
   // K elements summed in TMEM before the FP32 register promotion
   const int chunk_k = chunk_req > 0 ? chunk_req : kDefaultChunkK;
   p.chunk_kb = chunk_k / kGemmBK;
@@ -237,9 +294,11 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int gro
 }
 
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
-                int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req,
+                int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
                 cudaStream_t stream) {
-  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, bn_req, group_req, chunk_req);
+  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
+                                  cluster_req, variant == POOT_VARIANT_GEMM_TMA);
+  const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
   GemmArgs a;
   a.x = static_cast<const __half*>(x);
   a.w = static_cast<const __half*>(w);
@@ -252,8 +311,9 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   a.stages = plan.stages;
   a.group_m = plan.group_m;
   a.chunk_kb = plan.chunk_kb;
-  a.num_m_blocks = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
+  a.num_m_blocks = static_cast<int>((M + bm - 1) / bm);
   a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
+  if (plan.cluster == 4) a.num_n_blocks = (a.num_n_blocks + 1) / 2;  // tile pairs along N
   a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
   const int64_t tiles = int64_t(a.num_m_blocks) * a.num_n_blocks;
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
@@ -265,26 +325,41 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   std::memset(&tw, 0, sizeof(tw));
   std::memset(&ty, 0, sizeof(ty));
   if (variant == POOT_VARIANT_GEMM_TMA) {
-    if (!encode_2d(&tx, x, K, M, kGemmBK, kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tw, w, K, N, kGemmBK, static_cast<uint32_t>(plan.bn), CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_2d(&tx, x, K, M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, w, K, N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
+                   CU_TENSOR_MAP_SWIZZLE_128B))
       return cuda_fail(cudaErrorInvalidValue);
   }
   if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cuda_fail(cudaErrorInvalidValue);
 
-  const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
   cudaError_t e;
+  if (plan.cluster == 4) {
+    const int64_t clusters = st.max_clusters4;
+    const int grid = 4 * static_cast<int>(tiles < clusters ? tiles : clusters);
+    e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 4>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                         Layout::DYN_BYTES, stream, 4u, tx, tw, ty, a);
+    return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+  }
+  if (plan.cluster == 2) {
+    const int64_t pairs = st.sm_count / 2;
+    const int grid = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
+    e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 2>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                         Layout::DYN_BYTES, stream, 2u, tx, tw, ty, a);
+    return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+  }
+  const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
   switch (variant) {
     case POOT_VARIANT_GEMM_TMA:
-      e = launch(gemm_f16_tcgen05_kernel<kLoadTma>, dim3(grid), dim3(gemm_threads(kLoadTma)), Layout::DYN_BYTES,
-                 stream, tx, tw, ty, a);
+      e = launch(gemm_f16_tcgen05_kernel<kLoadTma, 1>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                 Layout::DYN_BYTES, stream, tx, tw, ty, a);
       break;
     case POOT_VARIANT_GEMM_CPASYNC:
-      e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4>, dim3(grid), dim3(gemm_threads(kLoadCpAsync4)),
+      e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1>, dim3(grid), dim3(gemm_threads(kLoadCpAsync4)),
                  Layout::DYN_BYTES, stream, tx, tw, ty, a);
       break;
     default:
-      e = launch(gemm_f16_tcgen05_kernel<kLoadReg16>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
+      e = launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
                  Layout::DYN_BYTES, stream, tx, tw, ty, a);
       break;
   }
@@ -368,6 +443,10 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
     return POOT_ERR_INVALID_ARG;
   if (o.gemm_group_m < 0) return POOT_ERR_INVALID_ARG;
   if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return POOT_ERR_INVALID_ARG;
+  if (o.gemm_cluster != 0 && o.gemm_cluster != 1 && o.gemm_cluster != 2 && o.gemm_cluster != 4)
+    return POOT_ERR_INVALID_ARG;
+  if (o.gemm_cluster > 1 && variant != POOT_VARIANT_AUTO && variant != POOT_VARIANT_GEMM_TMA)
+    return POOT_ERR_INVALID_ARG;
   if (variant == POOT_VARIANT_AUTO) {
     variant = choose_variant(x, w, M, N, K);
   } else if (!variant_applicable(variant, x, w, M, N, K)) {
@@ -396,7 +475,7 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
       return launch_gemv(variant, *st, x, w, b, y, M, N, K, gemv_wpr, stream);
     default:
       return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
-                         stream);
+                         o.gemm_cluster, stream);
   }
 }
 

@@ -139,6 +139,17 @@ def test_bad_gemm_k_chunk(chunk):
         L.POOT_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("cluster", [-1, 3, 8])
+def test_bad_gemm_cluster(cluster):
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_cluster=cluster), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
+def test_cluster_needs_the_tma_variant():
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64,
+                                L.options(L.VARIANT_GEMM_CPASYNC, gemm_cluster=2), 0) == L.POOT_ERR_INVALID_ARG
+
+
 def test_bad_gemm_group():
     assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_group_m=-1), 0) == \
         L.POOT_ERR_INVALID_ARG

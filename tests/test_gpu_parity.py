@@ -26,11 +26,11 @@ def _bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def _gpu(x, w, b, variant=L.VARIANT_AUTO, wpr=0, tile_n=0, group_m=0, k_chunk=0):
+def _gpu(x, w, b, variant=L.VARIANT_AUTO, wpr=0, tile_n=0, group_m=0, k_chunk=0, pair=0):
     xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
     y = torch.full((x.shape[0], w.shape[0]), float("nan"), dtype=torch.float16, device=DEV)
     L.linear(xd, wd, bd, y, variant=variant, gemv_warps_per_row=wpr, gemm_tile_n=tile_n,
-             gemm_group_m=group_m, gemm_k_chunk=k_chunk)
+             gemm_group_m=group_m, gemm_k_chunk=k_chunk, gemm_cluster=pair)
     torch.cuda.synchronize()
     assert L.poot_linear_device_status(0) == L.POOT_OK
     return _bits(y)
@@ -194,6 +194,38 @@ def test_k_chunk_promotion(k_chunk, variant):
     _check(x, w, b, _gpu(x, w, b, variant, k_chunk=k_chunk), exact_ints=True)
     xn, wn, bn = synth.make_inputs(260, 300, K, "normal", 81 + k_chunk)
     _check(xn, wn, bn, _gpu(xn, wn, bn, variant, k_chunk=k_chunk))
+
+
+# ---- CTA pairs (2-SM MMA) ------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 512, 256), (300, 520, 136), (1000, 700, 1000),
+                                   (129, 64, 64), (2047, 1000, 776)])
+@pytest.mark.parametrize("pair", [1, 2, 4])
+def test_cta_pair_exact(M, N, K, pair):
+    x, w, b = synth.make_inputs(M, N, K, "smallint", 40 + M % 97 + N % 13 + K)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, pair=pair), exact_ints=True)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 192, 224, 256])
+@pytest.mark.parametrize("pair", [2, 4])
+def test_cta_pair_tile_widths(tile_n, pair):
+    x, w, b = synth.make_inputs(700, 900, 200, "smallint", 50 + tile_n)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, tile_n=tile_n, pair=pair), exact_ints=True)
+
+
+@pytest.mark.parametrize("k_chunk", [64, 256, 4096])
+@pytest.mark.parametrize("pair", [2, 4])
+def test_cta_pair_chunks_normal(k_chunk, pair):
+    x, w, b = synth.make_inputs(600, 800, 1000, "normal", 55 + k_chunk)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, k_chunk=k_chunk, pair=pair))
+
+
+@pytest.mark.parametrize("pair", [2, 4])
+def test_cta_pair_many_tiles_per_pair(pair):
+    # more tiles than clusters: the persistent loop and both chunk buffers;
+    # N = 2560 / 128 = 20 tiles, and 2600 leaves an odd count for clusters of 4
+    for N in (2560, 2600):
+        x, w, b = synth.make_inputs(4096, N, 128, "smallint", 57 + N)
+        _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, tile_n=128, pair=pair), exact_ints=True)
 
 
 def test_more_tiles_than_sms():
