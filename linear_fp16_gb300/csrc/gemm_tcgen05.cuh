@@ -50,6 +50,11 @@ struct GemmArgs {
   int chunk_kb;  // K blocks accumulated in TMEM before promotion (>= 1)
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int tma_store;  // 1: TMA store of y; 0: plain stores (any pitch/alignment)
+  // 1: stages are filled, consumed and released in pairs, and a chunk's last
+  // pair is released through the chunk-complete barrier (TMA producer,
+  // clusters of at most two, even `stages`, every chunk an even number of at
+  // least `stages` K blocks); 0: one stage at a time
+  int paired;
 };
 
 constexpr int kGemmBM = 128;
@@ -272,34 +277,61 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
+        // Paired stages (args.paired): stages 2p and 2p+1 are filled together
+        // and released together through empty barrier p, and a chunk's last
+        // pair is released by the chunk-complete barrier instead (every chunk
+        // holds at least STAGES K blocks, so the fill at position STAGES - 2
+        // of chunk ch reuses the pair of chunk ch - 1's end).  ck: position
+        // in the chunk; ch: chunk count over this CTA's tiles (TMEM buffer and
+        // barrier phase).
+        const bool paired = CL <= 2 && args.paired != 0;
+        const int step = paired ? 2 : 1;
+        int ck = 0, ch = 0;
         for (int t = unit; t < args.num_tiles && ok; t += units) {
           int mb, nb;
           gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
           if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;  // this pair's N tile
-          for (int kb = 0; kb < num_kb; ++kb) {
-            if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-            const uint32_t fb = bar_full(stage);
-            if constexpr (PAIR) {
-              // both CTAs' bytes complete on the even CTA's barrier
-              const uint32_t fb0 = map_to_cta(fb, lead_rank);
-              if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
-              const int arow = mb * tile_rows + (int)rank * kGemmBM;
-              if constexpr (CL == 4) {
-                // half of the x tile, into this CTA and its counterpart in the other pair
-                const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
-                tma_load_2d_pair_multicast(stage_a(stage) + pair_id * (kGemmBM / 2) * 128u, &tm_x, fb0, kb * kGemmBK,
-                                           arow + (int)pair_id * (kGemmBM / 2), mask);
-              } else {
-                tma_load_2d_pair(stage_a(stage), &tm_x, fb0, kb * kGemmBK, arow);
-              }
-              tma_load_2d_pair(stage_b(stage), &tm_w, fb0, kb * kGemmBK, nb * BN + (int)rank * (BN / 2));
-            } else {
-              mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-              tma_load_2d(stage_a(stage), &tm_x, fb, kb * kGemmBK, mb * kGemmBM);
-              tma_load_2d(stage_b(stage), &tm_w, fb, kb * kGemmBK, nb * BN);
+          for (int kb = 0; kb < num_kb; kb += step) {
+            const uint32_t eb = paired ? bar_empty(stage >> 1) : bar_empty(stage);
+            if (paired && ck == STAGES - 2 && ch > 0) {
+              const int pc = ch - 1;
+              if (!mbar_wait(bar_cfull(pc & 1), (uint32_t)((pc >> 1) & 1), abort_flag)) { ok = false; break; }
+              mbar_arrive(eb);  // in place of the MMA's commit
             }
-            ++issued;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (!mbar_wait(eb, phase ^ 1u, abort_flag)) { ok = false; break; }
+            if (paired && leader && ck == 0) {
+              // the chunk's TMEM buffer must be drained before its first MMA;
+              // that MMA waits on this stage's full barrier, so the producer
+              // waits for the buffer before arming the barrier
+              if (!mbar_wait(bar_cempty(ch & 1), (uint32_t)(((ch >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+            }
+            for (int h = 0; h < step; ++h) {
+              const int st = stage + h, kc = (kb + h) * kGemmBK;
+              const uint32_t fb = bar_full(st);
+              if constexpr (PAIR) {
+                // both CTAs' bytes complete on the even CTA's barrier
+                const uint32_t fb0 = map_to_cta(fb, lead_rank);
+                if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
+                const int arow = mb * tile_rows + (int)rank * kGemmBM;
+                if constexpr (CL == 4) {
+                  // half of the x tile, into this CTA and its counterpart in the other pair
+                  const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
+                  tma_load_2d_pair_multicast(stage_a(st) + pair_id * (kGemmBM / 2) * 128u, &tm_x, fb0, kc,
+                                             arow + (int)pair_id * (kGemmBM / 2), mask);
+                } else {
+                  tma_load_2d_pair(stage_a(st), &tm_x, fb0, kc, arow);
+                }
+                tma_load_2d_pair(stage_b(st), &tm_w, fb0, kc, nb * BN + (int)rank * (BN / 2));
+              } else {
+                mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+                tma_load_2d(stage_a(st), &tm_x, fb, kc, mb * kGemmBM);
+                tma_load_2d(stage_b(st), &tm_w, fb, kc, nb * BN);
+              }
+            }
+            if (ck + step >= chunk_kb || kb + step >= num_kb) { ck = 0; ++ch; } else { ck += step; }
+            issued += step;
+            stage += step;
+            if (stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
         // Let the last loads land before the CTA can exit (their barrier
@@ -355,43 +387,93 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   } else if (warp == kGemmMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int buf = 0;
-      uint32_t buf_phase = 0;
-      bool ok = true;
-      for (int t = unit; t < args.num_tiles && ok; t += units) {
-        for (int c = 0; c < num_chunks && ok; ++c) {
-          if (!mbar_wait(bar_cempty(buf), buf_phase ^ 1u, abort_flag)) { ok = false; break; }
+      const bool paired = MODE == kLoadTma && CL <= 2 && args.paired != 0;
+      if (paired) {
+        // Two K blocks (two stages, eight MMAs) per iteration over all of
+        // this CTA's tiles, one commit each, every tcgen05 instruction
+        // unconditional: measured on GB300, a commit under a branch (even one
+        // never taken) or a wait and commit per four MMAs leaves gaps in the
+        // tensor pipe, eight MMAs per wait and commit do not.  A chunk's
+        // first MMA starts a fresh sum (accumulate off); its last pair
+        // commits to the chunk-complete barrier, which also frees the pair
+        // (the producers turn it into the pair's release), and the producer
+        // has already waited for the chunk's TMEM buffer before arming it.
+        const int my_tiles = unit < args.num_tiles ? (args.num_tiles - 1 - unit) / units + 1 : 0;
+        const long long total = (long long)my_tiles * num_kb;
+        int stage = 0;
+        uint32_t phase = 0;
+        int buf = 0;
+        int ck = 0, kb = 0;  // K block within the chunk and within the tile
+        for (long long g = 0; g < total; g += 2) {
+          if (!mbar_wait(bar_full(stage), phase, abort_flag)) break;
+          if (!mbar_wait(bar_full(stage + 1), phase, abort_flag)) break;
           tc_fence_after_sync();
+          const bool last = (ck + 2 >= chunk_kb) || (kb + 2 >= num_kb);
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kGemmMaxBN);
-          const int kb_end = min(num_kb, (c + 1) * chunk_kb);
-          for (int kb = c * chunk_kb; kb < kb_end; ++kb) {
-            if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
-            tc_fence_after_sync();
-            const uint64_t adesc = sdesc_kmajor_sw128(stage_a(stage));
-            const uint64_t bdesc = sdesc_kmajor_sw128(stage_b(stage));
-            const bool first = (kb == c * chunk_kb);
+          const uint64_t a0 = sdesc_kmajor_sw128(stage_a(stage)), b0 = sdesc_kmajor_sw128(stage_b(stage));
+          const uint64_t a1 = sdesc_kmajor_sw128(stage_a(stage + 1)), b1 = sdesc_kmajor_sw128(stage_b(stage + 1));
 #pragma unroll
-            for (int k = 0; k < kGemmBK / 16; ++k) {
-              // advance 16 elements = 32 bytes along K inside the swizzle row
-              if constexpr (PAIR)
-                umma_f16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
-              else
-                umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
-            }
-            // frees the stage (in both CTAs of a pair) when these MMAs finish
-            // (with CL = 4 in all four CTAs: a stage is refilled by both pairs)
-            if constexpr (CL == 4) umma_commit_pair(bar_empty(stage), 0xF);
-            else if constexpr (PAIR) umma_commit_pair(bar_empty(stage), 3);
-            else umma_commit(bar_empty(stage));
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          for (int k = 0; k < kGemmBK / 16; ++k) {
+            if constexpr (PAIR)
+              umma_f16_pair(d_tmem, a0 + 2u * k, b0 + 2u * k, IDESC, (ck == 0 && k == 0) ? 0u : 1u);
+            else
+              umma_f16(d_tmem, a0 + 2u * k, b0 + 2u * k, IDESC, (ck == 0 && k == 0) ? 0u : 1u);
           }
-          if (!ok) break;
-          // chunk sums ready for the epilogue(s)
-          if constexpr (PAIR) umma_commit_pair(bar_cfull(buf), (uint16_t)(3u << lead_rank));
-          else umma_commit(bar_cfull(buf));
-          if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
+#pragma unroll
+          for (int k = 0; k < kGemmBK / 16; ++k) {
+            if constexpr (PAIR)
+              umma_f16_pair(d_tmem, a1 + 2u * k, b1 + 2u * k, IDESC, 1u);
+            else
+              umma_f16(d_tmem, a1 + 2u * k, b1 + 2u * k, IDESC, 1u);
+          }
+          const uint32_t cbar = last ? bar_cfull(buf) : bar_empty(stage >> 1);
+          if constexpr (PAIR) umma_commit_pair(cbar, 3);
+          else umma_commit(cbar);
+          stage += 2;
+          if (stage == STAGES) { stage = 0; phase ^= 1u; }
+          buf ^= last ? 1 : 0;
+          ck = last ? 0 : ck + 2;
+          kb = (kb + 2 >= num_kb) ? 0 : kb + 2;
+        }
+      } else {
+        int stage = 0;
+        uint32_t phase = 0;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int t = unit; t < args.num_tiles && ok; t += units) {
+          for (int c = 0; c < num_chunks && ok; ++c) {
+            if (!mbar_wait(bar_cempty(buf), buf_phase ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kGemmMaxBN);
+            const int kb_end = min(num_kb, (c + 1) * chunk_kb);
+            for (int kb = c * chunk_kb; kb < kb_end; ++kb) {
+              if (!mbar_wait(bar_full(stage), phase, abort_flag)) { ok = false; break; }
+              tc_fence_after_sync();
+              const uint64_t adesc = sdesc_kmajor_sw128(stage_a(stage));
+              const uint64_t bdesc = sdesc_kmajor_sw128(stage_b(stage));
+              const bool first = (kb == c * chunk_kb);
+#pragma unroll
+              for (int k = 0; k < kGemmBK / 16; ++k) {
+                // advance 16 elements = 32 bytes along K inside the swizzle row
+                if constexpr (PAIR)
+                  umma_f16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                else
+                  umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+              }
+              // frees the stage (in both CTAs of a pair) when these MMAs finish
+              // (with CL = 4 in all four CTAs: a stage is refilled by both pairs)
+              if constexpr (CL == 4) umma_commit_pair(bar_empty(stage), 0xF);
+              else if constexpr (PAIR) umma_commit_pair(bar_empty(stage), 3);
+              else umma_commit(bar_empty(stage));
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            // chunk sums ready for the epilogue(s)
+            if constexpr (PAIR) umma_commit_pair(bar_cfull(buf), (uint16_t)(3u << lead_rank));
+            else umma_commit(bar_cfull(buf));
+            if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
+          }
         }
       }
       // every MMA this thread issued has finished before TMEM is released
@@ -419,6 +501,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;
       const int m0 = mb * tile_rows + (int)rank * kGemmBM, n0 = nb * BN;
+      // pull this warp's bias values into L1 now, so that the final epilogue
+      // reads them at L1 latency instead of waiting on memory once per box
+#pragma unroll
+      for (int g = 0; g < kGemmHalfCols / 32; ++g) {
+        const int col = n0 + col0 + g * 32 + lane;
+        if (g < ngroups && col < N) prefetch_l1(args.b + col);
+      }
       float acc[kGemmHalfCols];
 #pragma unroll
       for (int i = 0; i < kGemmHalfCols; ++i) acc[i] = 0.0f;
@@ -448,14 +537,20 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
       }
       if (!ok) break;
-      // final epilogue of this tile from registers
+      // final epilogue of this tile from registers; lane l of box g holds
+      // b[n0 + col0 + 32g + l], all boxes loaded together
+      unsigned short bias16[kGemmHalfCols / 32];
+#pragma unroll
+      for (int g = 0; g < kGemmHalfCols / 32; ++g) {
+        const int col = n0 + col0 + g * 32 + lane;
+        bias16[g] = (g < ngroups && col < N) ? __half_as_ushort(args.b[col]) : (unsigned short)0;
+      }
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         if (g < ngroups) {
           const int nc = n0 + col0 + g * 32;  // first column of this 32-column box
           // bias of the box: lane l holds b[nc + l]; broadcast by shuffles
-          const __half bl = (nc + lane < N) ? args.b[nc + lane] : __float2half_rn(0.0f);
-          const unsigned short blu = __half_as_ushort(bl);
+          const unsigned short blu = bias16[g];
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {

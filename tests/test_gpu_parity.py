@@ -228,6 +228,24 @@ def test_cta_pair_many_tiles_per_pair(pair):
         _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, tile_n=128, pair=pair), exact_ints=True)
 
 
+# Paired stages (two K blocks per MMA batch, released together, a chunk's
+# last pair released through the chunk-complete barrier) run when every chunk
+# holds an even number of at least `stages` K blocks; otherwise one stage at a
+# time.  Each case below runs more tiles than CTAs (or pairs), so chunk
+# counting continues across tiles.  K blocks of 64: 832 -> 13 (odd: one stage
+# at a time); 1152 -> 18 = 16 + a 2-block tail (too short: one at a time);
+# 1536 -> 24 = 16 + 8 (paired, with a tail chunk); 1536 with 384-element
+# chunks -> 4 chunks of 6 (paired at 6 stages, one at a time at 8); 1536 with
+# 192-element chunks -> chunks of 3 (odd: one at a time); 768 -> one chunk.
+@pytest.mark.parametrize("K,k_chunk", [(832, 0), (1152, 0), (1536, 0), (1536, 384), (1536, 192), (768, 0)])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_stage_pairing_boundaries(K, k_chunk, pair):
+    x, w, b = synth.make_inputs(520, 2048, K, "smallint", 90 + K + k_chunk)
+    _check(x, w, b, _gpu(x, w, b, L.VARIANT_GEMM_TMA, tile_n=64, k_chunk=k_chunk, pair=pair), exact_ints=True)
+    xn, wn, bn = synth.make_inputs(520, 2048, K, "normal", 91 + K + k_chunk)
+    _check(xn, wn, bn, _gpu(xn, wn, bn, L.VARIANT_GEMM_TMA, tile_n=256, k_chunk=k_chunk, pair=pair))
+
+
 def test_more_tiles_than_sms():
     # forces the persistent loop to take several tiles per CTA and both
     # TMEM accumulators
