@@ -119,27 +119,17 @@ __device__ __forceinline__ void gemm_tile_coords(int t, int num_m, int num_n, in
   nb = local / gsize;
 }
 
-// Copy producer: fills one operand tile (rows row0 .. row0+rows-1 of src,
-// K block at k0) in the 128-byte-swizzled K-major layout, zero outside
+// Register-copy producer (2-byte loads, any alignment): fills one operand
+// tile (rows row0 .. row0+rows-1 of src, K block at k0) in the
+// 128-byte-swizzled K-major layout, zero outside
 // [nrows) x [K).  Row r, 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
 // pt is the thread's index among the kGemmCopyThreads producer threads.
 template <int MODE>
 __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* __restrict__ src,
                                                int rows, int row0, int nrows, int K, int k0, int pt) {
   constexpr int T = kGemmCopyThreads;
-  if constexpr (MODE == kLoadCpAsync4) {
-    // 4-byte words: rows x 32 words; thread pt takes words pt, pt+T, ...
-    const int words = rows * 32;
-#pragma unroll 8
-    for (int wd = pt; wd < words; wd += T) {
-      const int r = wd >> 5, kw = wd & 31;
-      const int grow = row0 + r, k = k0 + 2 * kw;
-      const bool ok = (grow < nrows) && (k < K);  // K even: the pair is all in or all out
-      const __half* g = ok ? src + (size_t)grow * K + k : src;
-      const uint32_t d = dst_base + r * 128 + ((((kw >> 2) ^ (r & 7))) << 4) + ((kw & 3) << 2);
-      cp_async_4(d, g, ok ? 4u : 0u);
-    }
-  } else {
+  static_assert(MODE == kLoadReg16, "the cp.async producers use gemm_copy_rows_cp");
+  {
     // 16-byte chunks assembled from 2-byte loads: rows x 8 chunks, eight
     // chunks per thread in flight at a time.
     constexpr int PER = 8;
@@ -173,6 +163,33 @@ __device__ __forceinline__ void gemm_copy_tile(uint32_t dst_base, const __half* 
         }
       }
     }
+  }
+}
+
+// cp.async producer: fills one operand tile with WB-byte words (4, or 8 when
+// K % 4 == 0 and the operand is 8-byte aligned).  Copy warp cw of the three
+// takes every third group of RPI rows; within a warp instruction lane l
+// copies word l % LPR of row l / LPR, so one instruction moves 128 bytes of
+// each of its rows.  Row r, byte b lands at r*128 + (((b >> 4) ^ (r & 7)) << 4)
+// + (b & 15); words outside [nrows) x [K) are zero-filled.
+template <int WB>
+__device__ __forceinline__ void gemm_copy_rows_cp(uint32_t dst_base, const __half* __restrict__ src, int rows,
+                                                  int row0, int nrows, int K, int k0, int cw, int lane) {
+  constexpr int LPR = 128 / WB;  // lanes per row
+  constexpr int RPI = 32 / LPR;  // rows per warp instruction
+  constexpr int RSTEP = 3 * RPI;
+  const int wl = lane % LPR;
+  const int kk = k0 + wl * (WB / 2);
+  const bool kok = kk < K;  // K is a multiple of WB / 2 elements: a word is all in or all out
+  const uint32_t b = (uint32_t)(wl * WB);
+  int r = cw * RPI + lane / LPR;
+  const char* g = reinterpret_cast<const char*>(src) + ((size_t)(row0 + r) * K + kk) * 2;
+  const size_t gstep = (size_t)RSTEP * K * 2;
+  for (; r < rows; r += RSTEP, g += gstep) {
+    const bool ok = kok && (row0 + r < nrows);
+    const uint32_t d = dst_base + (uint32_t)r * 128u + ((((b >> 4) ^ (uint32_t)(r & 7))) << 4) + (b & 15u);
+    if constexpr (WB == 8) cp_async_8(d, ok ? (const void*)g : (const void*)src, ok ? 8u : 0u);
+    else cp_async_4(d, ok ? (const void*)g : (const void*)src, ok ? 4u : 0u);
   }
 }
 
@@ -349,39 +366,56 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       }
     } else {
       const int pt = threadIdx.x - kGemmProdWarp0 * 32;  // 0 .. kGemmCopyThreads-1
-      // copies of a stage complete LAG iterations after they are issued;
+      const int cw = pt >> 5;                             // copy warp 0 .. 2
+      // cp.async: copies of a stage complete LAG fills after they are issued;
       // LAG < STAGES (STAGES >= 4) keeps the ring from deadlocking
       constexpr int LAG = (MODE == kLoadCpAsync4) ? 3 : 0;
-      long long it = 0;
+      // 8-byte words when every row start and K slice is 8-byte aligned
+      const bool w8 = (args.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(args.x) | reinterpret_cast<uintptr_t>(args.w)) % 8 == 0);
+      int stage = 0, done_stage = 0;  // ring slot to fill next; slot whose copies complete next
+      uint32_t phase = 0;
+      int filled = 0;                 // fills issued (saturates at LAG)
       bool ok = true;
       for (int t = unit; t < args.num_tiles && ok; t += units) {
         int mb, nb;
         gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
-          const int stage = (int)(it % STAGES);
-          const uint32_t phase = (uint32_t)((it / STAGES) & 1);
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          gemm_copy_tile<MODE>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K,
-                               kb * kGemmBK, pt);
-          gemm_copy_tile<MODE>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
           if constexpr (MODE == kLoadCpAsync4) {
+            if (w8) {
+              gemm_copy_rows_cp<8>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<8>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+            } else {
+              gemm_copy_rows_cp<4>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<4>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+            }
             cp_async_commit();
-            if (it >= LAG) {
+            if (filled == LAG) {
               cp_async_wait_group<LAG>();
               fence_proxy_async_smem();
-              mbar_arrive(bar_full((int)((it - LAG) % STAGES)));
+              mbar_arrive(bar_full(done_stage));
+              if (++done_stage == STAGES) done_stage = 0;
+            } else {
+              ++filled;
             }
           } else {
+            gemm_copy_tile<MODE>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K,
+                                 kb * kGemmBK, pt);
+            gemm_copy_tile<MODE>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
             fence_proxy_async_smem();
             mbar_arrive(bar_full(stage));
           }
-          ++it;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       if constexpr (MODE == kLoadCpAsync4) {
+        // the last `filled` fills (at most LAG) have not been signalled yet
         cp_async_wait_all();
         fence_proxy_async_smem();
-        for (long long j = (it > LAG ? it - LAG : 0); j < it; ++j) mbar_arrive(bar_full((int)(j % STAGES)));
+        for (int j = 0; j < filled; ++j) {
+          mbar_arrive(bar_full(done_stage));
+          if (++done_stage == STAGES) done_stage = 0;
+        }
       }
     }
   } else if (warp == kGemmMmaWarp) {

@@ -249,15 +249,26 @@ struct GemmPlan {
 // extrapolated below it.  Ties go to the wider tile.
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, int bn_req, int group_req,
                    int chunk_req, int cluster_req, bool tma) {
-  // CTA pairs (2-SM MMA) for large problems; single CTAs when M is small (a
-  // pair's 256-row tile would be mostly empty) or the operands need copies.
+  // CTA pairs (2-SM MMA) from M = 256 (one full pair tile); single CTAs
+  // when M is smaller, for short K in one wave, or when the operands need
+  // copies.
   // Clusters of two pairs sharing the x tile cut L2 reads by a fifth but fit
   // only 36 clusters (144 SMs); interleaved timing on GB300 showed no gain
   // over pairs on 4096^3 and 8192x14336x4096, so they are opt-in.
   int cluster = 1;
+  bool short_k_wave = false;
   if (tma) {
+    // short K in one wave of 128 x 64 single-CTA tiles: the pair's two
+    // cluster barriers (about 0.5 us each) outweigh its gain (1024 x 1024 x
+    // 768 on GB300: 6.5 us single, 8.0 us in pairs)
+    const int64_t single64 = ((M + kGemmBM - 1) / kGemmBM) * ((N + 63) / 64);
+    short_k_wave = (K + kGemmBK - 1) / kGemmBK <= 16 && single64 <= sms;
+    // below 512 rows, 256-row pair tiles only where they pad M no more than
+    // 128-row tiles do (384 x 4096 x 4096: 19.9 us single, 20.9 us in
+    // pairs; 640 x 4096 x 4096: 29.0 us single, 24.2 us in pairs)
+    const bool pair_rows = (M + 255) / 256 * 2 == (M + 127) / 128 || M >= 512;
     if (cluster_req != 0) cluster = cluster_req;
-    else if (M >= 512 && N >= 512) cluster = 2;
+    else if (M >= 256 && N >= 256 && pair_rows && !short_k_wave) cluster = 2;
   }
   const bool pair = cluster >= 2;
   const int64_t bm = pair ? 2 * kGemmBM : kGemmBM;
@@ -278,6 +289,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, 
     if (cost < best) { best = cost; best_bn = bn; }
   }
   if (bn_req != 0) best_bn = bn_req;
+  else if (cluster == 1 && short_k_wave) best_bn = 64;  // most CTAs loading at once
   GemmPlan p;
   p.cluster = cluster;
   p.pair = pair;

@@ -203,6 +203,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 // 16 bytes, L2 only; src_bytes (0 or 16) copied, the rest zero-filled.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
