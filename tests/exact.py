@@ -149,3 +149,67 @@ def same_values(a, b) -> bool:
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     return bool(np.all((a == b) | (np.isnan(a) & np.isnan(b))))
+
+
+# ---- formats other than binary16 -------------------------------------------------
+# (p significand bits with the hidden bit, minimum normal exponent, maximum exponent)
+FORMATS = {"f16": (11, -14, 15), "bf16": (8, -126, 127)}
+
+
+def rn_format(q, fmt: str) -> float:
+    """Round an exact rational (or float) to binary16 / bfloat16, nearest even.
+
+    Returns a Python float (exact for both formats); +-inf on overflow.
+    """
+    p, emin, emax = FORMATS[fmt]
+    q = Fraction(q)
+    if q == 0:
+        return 0.0
+    sign = -1.0 if q < 0 else 1.0
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    qe = max(e, emin) - (p - 1)
+    n = a / Fraction(2) ** qe
+    whole = n.numerator // n.denominator
+    rem = n - whole
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and whole % 2 == 1):
+        whole += 1
+    val = Fraction(whole) * Fraction(2) ** qe
+    maxv = (2 - Fraction(2) ** (1 - p)) * Fraction(2) ** emax
+    if val > maxv:
+        return sign * math.inf
+    return sign * float(val)
+
+
+def bf16_bits_to_float(h) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 values (bfloat16 is binary32's upper half)."""
+    h = np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16
+    return h.view(np.float32).astype(np.float64)
+
+
+def float_to_bits(v, fmt: str) -> np.ndarray:
+    """Exact binary16 / bfloat16 values (float64) -> their bit patterns."""
+    v = np.asarray(v, dtype=np.float64)
+    if fmt == "f16":
+        return v.astype(np.float16).view(np.uint16)
+    f = v.astype(np.float32)
+    assert np.array_equal(f.astype(np.float64)[np.isfinite(v)], v[np.isfinite(v)])
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def parse_chain_golden(name: str):
+    """Read 'case <dtype> <op> <t> <y>' lines of an epilogue fixture."""
+    cases = []
+    with open(os.path.join(GOLDEN_DIR, name)) as fh:
+        for raw in fh:
+            line = raw.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            assert tok[0] == "case" and len(tok) == 5, line
+            cases.append((tok[1], tok[2], float(tok[3]), float(tok[4])))
+    return cases
