@@ -51,6 +51,21 @@ METRIC = "TFLOP/s of y=FP16(x·Wᵀ)+b per M×N×K; % of FP16 tensor peak / HBM 
 CPU_SAMPLE_SECONDS = 10.0
 
 
+# Widened-contraction forms for --contract: (head dtype, out_f32, bias, steps);
+# a step is an activation name or (op, "r") for an [M,N] operand drawn N(0,1).
+CONTRACT_FORMS = {
+    "bf16": ("bf16", False, True, []),
+    "f32out": ("f16", True, True, []),
+    "nobias": ("f16", False, False, []),
+    "silu": ("f16", False, True, ["silu"]),
+    "gelu_tanh": ("f16", False, True, ["gelu_tanh"]),
+    "gelu_erf": ("f16", False, True, ["gelu_erf"]),
+    "residual": ("f16", False, True, [("add", "r")]),
+    "swiglu": ("f16", False, True, ["silu", ("mul", "r")]),
+    "bf16_swiglu": ("bf16", False, True, ["silu", ("mul", "r")]),
+}
+
+
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -66,6 +81,8 @@ def parse_args():
     p.add_argument("--group-m", type=int, default=0, help="GEMM tile-order group (0 = automatic)")
     p.add_argument("--no-graph", action="store_true", help="launch the timed steps eagerly")
     p.add_argument("--k-chunk", type=int, default=0, help="GEMM TMEM chunk along K (0 = automatic)")
+    p.add_argument("--contract", default="", choices=[""] + sorted(CONTRACT_FORMS),
+                   help="time a widened-contraction form (poot_contract) instead of the plain linear")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -500,11 +517,128 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def run_contract(args, rank, world, local):
+    """Time one widened-contraction form (kernel throughput, graph-timed)."""
+    import ctypes
+    import torch
+    import linear_fp16_gb300 as L
+    from linear_fp16_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    dt_name, out_f32, with_bias, steps = CONTRACT_FORMS[args.contract]
+    tdt = torch.bfloat16 if dt_name == "bf16" else torch.float16
+    wl = synth.WORKLOADS[args.workload]
+    M, N, K = wl.M, wl.N, wl.K
+    x_h, w_h, b_h = synth.workload_inputs(args.workload, seed_offset=0)
+    x, w, b = (t.to(dev).to(tdt) for t in (x_h, w_h, b_h))
+    g = torch.Generator(device="cpu").manual_seed(wl.seed + 77)
+    n_ops = sum(1 for st in steps if not isinstance(st, str))
+    ydt = torch.float32 if out_f32 else tdt
+    ybytes = 4 if out_f32 else 2
+    working_set = 2 * (M * K + N * K + N) + ybytes * M * N + 2 * M * N * n_ops
+    copies = 1 if working_set >= 3 * L2_BYTES else min(64, -(-3 * L2_BYTES // working_set))
+    sets = []
+    for c in range(copies):
+        xs, ws, bs = (x, w, b) if c == 0 else (x.clone(), w.clone(), b.clone())
+        ops = [torch.randn((M, N), generator=g).to(dev).to(tdt) for _ in range(n_ops)]
+        spec = L.ContractionSpec()
+        spec.dtype = L.DTYPE_BF16 if dt_name == "bf16" else L.DTYPE_F16
+        spec.out_f32 = int(out_f32)
+        spec.num_steps = len(steps)
+        k = 0
+        for i, st in enumerate(steps):
+            name = st if isinstance(st, str) else st[0]
+            spec.steps[i].op = L.binding.EP_CODES[name]
+            if not isinstance(st, str):
+                spec.steps[i].operand = ops[k].data_ptr()
+                spec.steps[i].ld = N
+                k += 1
+        y = torch.empty((M, N), dtype=ydt, device=dev)
+        sets.append((xs, ws, bs if with_bias else None, y, ops, spec))
+    opts = L.options(L.VARIANT_AUTO, 0, args.tile_n, args.group_m, args.k_chunk)
+    lib = L.load_library()
+
+    def step(i, sh):
+        xs, ws, bs, y, _, spec = sets[i % copies]
+        rc = lib.poot_contract(xs.data_ptr(), ws.data_ptr(), bs.data_ptr() if bs is not None else None,
+                               y.data_ptr(), M, N, K, ctypes.byref(spec), ctypes.byref(opts), sh)
+        if rc != 0:
+            raise RuntimeError(f"poot_contract: {L.poot_linear_status_string(rc)}")
+
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        step(i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream().cuda_stream
+        for i in range(args.steps):
+            step(args.warmup + i, cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    wall1 = time.time()
+    clocks = None
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary(wall0, wall1)
+    step_ms = max_over_ranks(dist, t0.elapsed_time(t1) / args.steps, dev)
+    if L.poot_linear_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    flops = 2.0 * M * N * K
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    alg_bytes = 2 * (M * K + N * K + (N if with_bias else 0)) + ybytes * M * N + 2 * M * N * n_ops
+    line = {
+        "metric": METRIC, "value": world * achieved, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt_name, "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "N": N, "K": K, "dist": wl.dist, "seed": wl.seed,
+                   "accumulate": "f32", "contract": args.contract, "out": "f32" if out_f32 else dt_name,
+                   "bias": with_bias, "steps": [st if isinstance(st, str) else st[0] for st in steps],
+                   "l2": "inputs larger than L2" if copies == 1 else f"{copies} rotating copies",
+                   "timing": "CUDA graph of the K steps, replayed between two events",
+                   "hbm_gbs_algorithmic": alg_bytes / (step_ms * 1e-3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{src} dense bf16 burst",
+                     "traffic": None, "kernel": "gemm_f16_tcgen05_kernel<tma, general>",
+                     "kernel_ms": step_ms, "algorithmic_per_launch": flops},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.contract:
+        return run_contract(args, rank, world, local)
     return run_ours(args, rank, world, local)
 
 

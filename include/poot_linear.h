@@ -167,6 +167,76 @@ POOT_API const char* poot_linear_last_cuda_error(void);
  */
 POOT_API int poot_linear_device_status(poot_stream_t stream);
 
+/* ---- The widened contraction ---------------------------------------------
+ *
+ * "ML compiler internals", section "The OpKind vocabulary": the
+ * ContractionEpilogue row (a dense contraction and the single-use
+ * pointwise chain that consumes it; the head's result keeps its dtype, a
+ * BF16 head rounds to BF16 before the first step reads it, and every step
+ * rounds through it) and the DenseContraction row (an f32 result); section
+ * "SwiGLU and GeLU FFN" (SiLU and GELU are compositions of the Neg, Exp,
+ * Add, Div, Mul and Erf primitives).  For every output element
+ *
+ *   S = sum_k x[m,k] W[n,k]            products in FP32, any summation order
+ *   out_f32:  y = S, or RN32(S + b[n]) with a bias   (float32 y, no steps)
+ *   else:     t = RN_h(S); t = RN_h(t + b[n]) when b != NULL;
+ *             each step:  t = step(t);  y = t         (head dtype h)
+ *
+ * where every primitive of a step rounds to h:
+ *   POOT_EP_ADD        t + r[m,n]
+ *   POOT_EP_MUL        t * r[m,n]
+ *   POOT_EP_SILU       t / (1 + exp(-t))                 (Neg, Exp, Add, Div)
+ *   POOT_EP_GELU_TANH  t / (1 + exp(-c2 (t + c1 t^3))),   c1 = RN_h(0.044715),
+ *                      c2 = RN_h(2 sqrt(2/pi))            (Mul, Add, Neg, Exp, Div)
+ *   POOT_EP_GELU_ERF   0.5 (t (1 + erf(c3 t))),           c3 = RN_h(1/sqrt 2)
+ *                                                          (Mul, Erf, Add)
+ * in the order the steps are listed.  Exp and Erf are evaluated in FP32 and
+ * rounded to h; every other primitive equals the correctly rounded h result.
+ */
+enum poot_dtype { POOT_DTYPE_F16 = 0, POOT_DTYPE_BF16 = 1 };
+enum poot_epilogue_op {
+    POOT_EP_ADD = 1,
+    POOT_EP_MUL = 2,
+    POOT_EP_SILU = 3,
+    POOT_EP_GELU_TANH = 4,
+    POOT_EP_GELU_ERF = 5
+};
+#define POOT_EPILOGUE_MAX_STEPS 4
+
+typedef struct poot_epilogue_step {
+    int op;                  /* POOT_EP_* */
+    const void* operand;     /* ADD, MUL: device pointer to r, [M, ld] row-major
+                                in the head dtype (2-byte aligned, read only,
+                                not overlapping y); NULL for the others */
+    int64_t ld;              /* row pitch of r in elements (>= N); 0 means N */
+} poot_epilogue_step;
+
+typedef struct poot_contraction_spec {
+    int dtype;               /* POOT_DTYPE_F16 or POOT_DTYPE_BF16: x, W, b, the
+                                step operands and (unless out_f32) y */
+    int out_f32;             /* 1: y is float32 (4-byte aligned) and holds the
+                                unrounded sum (+ b), num_steps must be 0 */
+    int num_steps;           /* 0 .. POOT_EPILOGUE_MAX_STEPS */
+    poot_epilogue_step steps[POOT_EPILOGUE_MAX_STEPS];
+} poot_contraction_spec;
+
+/*
+ * y = the widened contraction of x [M,K] and W [N,K] ([out, in], read in
+ * place) with the optional bias b [N] (NULL: none) under `spec`, on
+ * `stream`.  All pointers are device pointers; y is [M,N] row-major.
+ * Runs on the tcgen05 GEMM for every M (the GEMV kernels serve only
+ * poot_linear_f16).  `opts` may be NULL; its GEMV fields and variants are
+ * ignored except the GEMM ones.  Asynchronous; the caller owns every
+ * buffer; the library allocates nothing.
+ * Errors: POOT_ERR_INVALID_ARG for a NULL spec, x, w or y, K == 0, a bad
+ * dtype, step code, step count, NULL operand or ld < N, steps with out_f32,
+ * or y overlapping x, W, b or an operand; POOT_ERR_MISALIGNED for a pointer
+ * below its element alignment; otherwise as poot_linear_f16.
+ */
+POOT_API int poot_contract(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N,
+                           int64_t K, const poot_contraction_spec* spec, const poot_linear_options* opts,
+                           poot_stream_t stream);
+
 /* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
 POOT_API int poot_linear_version(void);
 

@@ -1,7 +1,9 @@
 """GB300-native FP16 linear: y = FP16(x . W^T) + b on sm_103a.
 
-``linear(x, w, b)`` is the tensor-level call; the C entry points of
-include/poot_linear.h are mirrored one to one in ``binding``.
+``linear(x, w, b)`` is the tensor-level call, and ``contract`` the widened
+contraction (bfloat16 heads, no bias, FP32 output, fused epilogue steps);
+the C entry points of include/poot_linear.h are mirrored one to one in
+``binding``.
 """
 from .binding import (  # noqa: F401
     GEMV_MAX_M, Options, options, POOT_ERR_CUDA, POOT_ERR_DEVICE_TIMEOUT, POOT_ERR_INVALID_ARG,
@@ -11,6 +13,8 @@ from .binding import (  # noqa: F401
     library_path, linear, load_library, poot_linear_device_status, poot_linear_f16,
     poot_linear_f16_ex, poot_linear_f16_variant, poot_linear_last_cuda_error,
     poot_linear_status_string, poot_linear_version, variant_for,
+    ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,
+    EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract,
 )
 
 __version__ = "0.1.0"

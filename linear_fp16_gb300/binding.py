@@ -37,6 +37,17 @@ VARIANT_NAMES = {
 }
 GEMV_MAX_M = 16
 
+# the widened contraction (poot_contract)
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+EP_ADD = 1
+EP_MUL = 2
+EP_SILU = 3
+EP_GELU_TANH = 4
+EP_GELU_ERF = 5
+EPILOGUE_MAX_STEPS = 4
+EP_CODES = {"add": EP_ADD, "mul": EP_MUL, "silu": EP_SILU, "gelu_tanh": EP_GELU_TANH, "gelu_erf": EP_GELU_ERF}
+
 
 
 class Options(ctypes.Structure):
@@ -51,6 +62,17 @@ def options(variant: int = -1, gemv_warps_per_row: int = 0, gemm_tile_n: int = 0
     return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster)
 
 
+class EpilogueStep(ctypes.Structure):
+    """struct poot_epilogue_step."""
+    _fields_ = [("op", ctypes.c_int), ("operand", ctypes.c_void_p), ("ld", ctypes.c_int64)]
+
+
+class ContractionSpec(ctypes.Structure):
+    """struct poot_contraction_spec."""
+    _fields_ = [("dtype", ctypes.c_int), ("out_f32", ctypes.c_int), ("num_steps", ctypes.c_int),
+                ("steps", EpilogueStep * EPILOGUE_MAX_STEPS)]
+
+
 # (name, restype, argtypes) of every exported symbol
 _VP = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -63,6 +85,8 @@ EXPORTS = {
     "poot_linear_last_cuda_error": (ctypes.c_char_p, []),
     "poot_linear_device_status": (ctypes.c_int, [_VP]),
     "poot_linear_version": (ctypes.c_int, []),
+    "poot_contract": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.POINTER(ContractionSpec),
+                                     ctypes.POINTER(Options), _VP]),
 }
 
 _lock = threading.Lock()
@@ -133,6 +157,12 @@ def poot_linear_version() -> int:
     return load_library().poot_linear_version()
 
 
+def poot_contract(x: int, w: int, b: int, y: int, M: int, N: int, K: int, spec, opts, stream: int) -> int:
+    """spec: a ContractionSpec; opts: an Options instance or None; b may be 0 (no bias)."""
+    ref = ctypes.byref(opts) if opts is not None else None
+    return load_library().poot_contract(x, w, b or None, y, M, N, K, ctypes.byref(spec), ref, stream)
+
+
 status_string = poot_linear_status_string
 last_cuda_error = poot_linear_last_cuda_error
 
@@ -194,3 +224,62 @@ def variant_for(x, w, b, y) -> int:
     M, K = x.shape
     N = w.shape[0]
     return poot_linear_f16_variant(x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), M, N, K)
+
+
+# ---- tensor-level widened contraction ------------------------------------
+def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_tile_n: int = 0,
+             gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0, variant: int = VARIANT_AUTO,
+             stream=None):
+    """The widened contraction (include/poot_linear.h, poot_contract).
+
+    x [M,K], w [N,K] and b [N] (or None) are float16 or bfloat16 CUDA
+    tensors of one dtype (the head dtype).  ``steps``: a sequence of
+    "silu", "gelu_tanh", "gelu_erf" or ("add" | "mul", r) with r an [M,N]
+    tensor (row pitch from its stride) of the head dtype.  Returns y [M,N]:
+    float32 with ``out_f32`` (no steps then), else the head dtype.
+    """
+    import torch
+    dt = x.dtype
+    if dt not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"x must be float16 or bfloat16, got {dt}")
+    for name, t in (("x", x), ("w", w)) + ((("b", b),) if b is not None else ()):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of x's dtype")
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"x [M,K] and w [N,K] expected, got {tuple(x.shape)} {tuple(w.shape)}")
+    M, K = x.shape
+    N = w.shape[0]
+    if b is not None and tuple(b.shape) != (N,):
+        raise ValueError(f"b must be [N], got {tuple(b.shape)}")
+    steps = list(steps)
+    if len(steps) > EPILOGUE_MAX_STEPS:
+        raise ValueError(f"at most {EPILOGUE_MAX_STEPS} epilogue steps")
+    spec = ContractionSpec()
+    spec.dtype = DTYPE_BF16 if dt == torch.bfloat16 else DTYPE_F16
+    spec.out_f32 = int(bool(out_f32))
+    spec.num_steps = len(steps)
+    for i, st in enumerate(steps):
+        name, operand = (st, None) if isinstance(st, str) else st
+        if name not in EP_CODES:
+            raise ValueError(f"unknown epilogue step {name!r}")
+        spec.steps[i].op = EP_CODES[name]
+        if name in ("add", "mul"):
+            r = operand
+            if (not isinstance(r, torch.Tensor) or r.dtype != dt or not r.is_cuda or r.dim() != 2
+                    or tuple(r.shape) != (M, N) or r.stride(1) != 1):
+                raise ValueError(f"step {name}: an [M,N] CUDA tensor of x's dtype with unit column stride")
+            spec.steps[i].operand = r.data_ptr()
+            spec.steps[i].ld = r.stride(0)
+    ydt = torch.float32 if out_f32 else dt
+    if out is None:
+        out = torch.empty((M, N), dtype=ydt, device=x.device)
+    elif out.dtype != ydt or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [M, N] {ydt} tensor")
+    with torch.cuda.device(x.device):
+        s = torch.cuda.current_stream(x.device) if stream is None else stream
+        rc = poot_contract(x.data_ptr(), w.data_ptr(), b.data_ptr() if b is not None else 0, out.data_ptr(),
+                           M, N, K, spec, options(variant, 0, gemm_tile_n, gemm_group_m, gemm_k_chunk,
+                                                  gemm_cluster), s.cuda_stream)
+    if rc != POOT_OK:
+        raise PootLinearError(rc, "poot_contract")
+    return out

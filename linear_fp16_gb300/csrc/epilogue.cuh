@@ -1,0 +1,115 @@
+// Device helpers of the widened contraction's epilogue ("ML compiler
+// internals", section "The OpKind vocabulary": the ContractionEpilogue row —
+// the head's result keeps its dtype and every step of the pointwise chain
+// rounds through it — and section "SwiGLU and GeLU FFN": SiLU and GELU are
+// compositions of the Neg, Exp, Add, Div, Mul and Erf primitives).
+//
+// Every primitive below is evaluated in FP32 and rounded to the head dtype
+// (binary16 or bfloat16).  For +, *, / of two head-dtype values FP32 has at
+// least 2p + 2 significand bits (p = 11 or 8), so FP32-then-round equals
+// the correctly rounded head result (the double rounding is innocuous);
+// the IEEE-rounded intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn) keep the
+// compiler from fusing two primitives into one rounding.  Exp and Erf use
+// expf / erff and then round.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace poot {
+
+enum EpiDtype : int { kEpiF16 = 0, kEpiBf16 = 1 };
+enum EpiOp : int { kEpAdd = 1, kEpMul = 2, kEpSilu = 3, kEpGeluTanh = 4, kEpGeluErf = 5 };
+constexpr int kEpiMaxSteps = 4;
+
+// round one FP32 value to the head dtype and back (exact widening)
+__device__ __forceinline__ float ep_rh(float v, int dt) {
+  return dt == kEpiBf16 ? __bfloat162float(__float2bfloat16_rn(v)) : __half2float(__float2half_rn(v));
+}
+
+// two FP32 values rounded to the head dtype, packed low = first
+__device__ __forceinline__ uint32_t ep_pack(float a, float b, int dt) {
+  if (dt == kEpiBf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// a packed pair of head-dtype values, widened exactly to FP32
+__device__ __forceinline__ float2 ep_unpack(uint32_t u, int dt) {
+  if (dt == kEpiBf16) return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
+__device__ __forceinline__ float ep_widen(uint16_t bits, int dt) {
+  if (dt == kEpiBf16) return __uint_as_float((uint32_t)bits << 16);
+  return __half2float(__ushort_as_half(bits));
+}
+
+// x / (1 + exp(-x)) over Neg, Exp, Add, Div
+__device__ __forceinline__ float ep_silu(float t, int dt) {
+  const float e = ep_rh(expf(-t), dt);  // -t is exact
+  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
+  return ep_rh(__fdiv_rn(t, d), dt);
+}
+
+// the tanh approximation in its sigmoid form: x / (1 + exp(-c2 (x + c1 x^3)))
+// c1 = RN(0.044715), c2 = RN(2 sqrt(2/pi)); the FP32 literals are within
+// 2^-24 relative of the exact constants, far from a rounding boundary of
+// either head dtype, so rounding them gives the same head values
+__device__ __forceinline__ float ep_gelu_tanh(float t, int dt) {
+  const float c1 = ep_rh(0.044715f, dt);
+  const float c2 = ep_rh(1.5957691216057308f, dt);
+  const float s = ep_rh(__fmul_rn(t, t), dt);
+  const float c = ep_rh(__fmul_rn(s, t), dt);
+  const float u = ep_rh(__fmul_rn(c1, c), dt);
+  const float v = ep_rh(__fadd_rn(t, u), dt);
+  const float z = ep_rh(__fmul_rn(c2, v), dt);
+  const float e = ep_rh(expf(-z), dt);
+  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
+  return ep_rh(__fdiv_rn(t, d), dt);
+}
+
+// 0.5 x (1 + erf(x / sqrt 2)) over Mul, Erf, Add; c3 = RN(1/sqrt 2)
+__device__ __forceinline__ float ep_gelu_erf(float t, int dt) {
+  const float c3 = ep_rh(0.70710678118654752f, dt);
+  const float s = ep_rh(__fmul_rn(c3, t), dt);
+  const float e = ep_rh(erff(s), dt);
+  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
+  const float p = ep_rh(__fmul_rn(t, d), dt);
+  return ep_rh(__fmul_rn(0.5f, p), dt);
+}
+
+__device__ __forceinline__ float ep_activation(int op, float t, int dt) {
+  switch (op) {
+    case kEpSilu: return ep_silu(t, dt);
+    case kEpGeluTanh: return ep_gelu_tanh(t, dt);
+    case kEpGeluErf: return ep_gelu_erf(t, dt);
+    default: return t;
+  }
+}
+
+// Eight consecutive elements (bits) of row `row`, columns c .. c+7, of an
+// [M, ld] operand; zero outside [M) x [N).  `vec`: base 16-byte aligned and
+// ld % 8 == 0 (c is a multiple of 8), so a full chunk is one 16-byte load.
+__device__ __forceinline__ uint4 ep_load8(const uint16_t* __restrict__ base, long long ld, int row, int M, int c,
+                                          int N, bool vec) {
+  uint4 r = make_uint4(0u, 0u, 0u, 0u);
+  if (row >= M) return r;
+  const uint16_t* p = base + (size_t)row * (size_t)ld + c;
+  if (vec && c + 8 <= N) return __ldg(reinterpret_cast<const uint4*>(p));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t e = (c + j < N) ? (uint32_t)__ldg(p + j) : 0u;
+    w[j >> 1] |= e << ((j & 1) * 16);
+  }
+  r.x = w[0]; r.y = w[1]; r.z = w[2]; r.w = w[3];
+  return r;
+}
+
+}  // namespace poot

@@ -32,6 +32,7 @@
 // ulps of a sequential FP32 sum on cancelling sums as well.
 #pragma once
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace poot {
@@ -55,7 +56,30 @@ struct GemmArgs {
   // clusters of at most two, even `stages`, every chunk an even number of at
   // least `stages` K blocks); 0: one stage at a time
   int paired;
+  // The widened contraction (poot_contract).  general == 0: the plain
+  // binary16 epilogue y = RN16(RN16(sum) + b).  general == 1: head dtype
+  // `dtype`, optional bias, FP32 output or the epilogue steps.
+  int general;
+  int dtype;     // EpiDtype: x, W, b, step operands and y
+  int out_f32;   // y32 = sum (+ b in FP32); no head rounding, no steps
+  int has_bias;  // b is read (always 1 on the plain path)
+  int y_vec;     // out_f32: 16-byte stores (y32 16-byte aligned, N % 4 == 0)
+  int num_steps;
+  int ep_op[kEpiMaxSteps];
+  int ep_vec[kEpiMaxSteps];  // operand 16-byte aligned with ld % 8 == 0
+  const uint16_t* ep_ptr[kEpiMaxSteps];
+  long long ep_ld[kEpiMaxSteps];
+  float* y32;
 };
+
+// Activation step over the 16 packed pairs of one 32-column box (kept out of
+// line: the packed pairs pass through local memory only on this path).
+__device__ __noinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) {
+  for (int i = 0; i < 16; ++i) {
+    const float2 t = ep_unpack(v[i], dt);
+    v[i] = ep_pack(ep_activation(op, t.x, dt), ep_activation(op, t.y, dt), dt);
+  }
+}
 
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;        // one 128-byte swizzle row of binary16
@@ -207,7 +231,10 @@ __device__ __forceinline__ void gemm_copy_rows_cp(uint32_t dst_base, const __hal
 // both, so a CTA reads 24 KB per stage from L2 instead of 32 KB.  A stage is
 // refilled only after both pairs' MMAs released it (each "empty" barrier
 // counts one multicast commit from each pair).
-template <int MODE, int CL>
+// GEN: the widened contraction's epilogue (head dtype, optional bias, FP32
+// output, epilogue steps) is compiled in; without it the kernel has only the
+// plain binary16 epilogue and ignores the fields that select the rest.
+template <int MODE, int CL, bool GEN = false>
 __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     gemm_f16_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x,
                             const __grid_constant__ CUtensorMap tm_w,
@@ -219,7 +246,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const int BN = args.bn;
   const int STAGES = args.stages;
   const int STAGE_BYTES = gemm_stage_bytes(BN, PAIR);
-  const uint32_t IDESC = idesc_f16_f32acc(PAIR ? 2 * kGemmBM : kGemmBM, (uint32_t)BN);
+  // A and B both binary16, or both bfloat16 (bits 7-9 and 10-12: format 1)
+  const uint32_t IDESC = idesc_f16_f32acc(PAIR ? 2 * kGemmBM : kGemmBM, (uint32_t)BN) |
+                         ((GEN && args.dtype == kEpiBf16) ? ((1u << 7) | (1u << 10)) : 0u);
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
   const uint32_t rank = crank & 1u;               // row half of the pair's tile
   const uint32_t pair_id = crank >> 1;            // CL = 4: which of the two N tiles
@@ -540,7 +569,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         const int col = n0 + col0 + g * 32 + lane;
-        if (g < ngroups && col < N) prefetch_l1(args.b + col);
+        if ((!GEN || args.has_bias) && g < ngroups && col < N) prefetch_l1(args.b + col);
       }
       float acc[kGemmHalfCols];
 #pragma unroll
@@ -577,7 +606,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         const int col = n0 + col0 + g * 32 + lane;
-        bias16[g] = (g < ngroups && col < N) ? __half_as_ushort(args.b[col]) : (unsigned short)0;
+        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(args.b[col])
+                                                                         : (unsigned short)0;
       }
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
@@ -585,15 +615,81 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           const int nc = n0 + col0 + g * 32;  // first column of this 32-column box
           // bias of the box: lane l holds b[nc + l]; broadcast by shuffles
           const unsigned short blu = bias16[g];
-          uint32_t packed[16];
+          const int dt = GEN ? args.dtype : (int)kEpiF16;
+          if (GEN && args.out_f32) {
+            // FP32 output: the sum (+ b rounded once in FP32); lane = row,
+            // its 32 consecutive columns stored directly
+            const int row = m0 + q * 32 + lane;
+            float* yr = args.y32 + (size_t)(row < M ? row : 0) * N + nc;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            // proj = RN16(acc) for two columns, then y = RN16(proj + b)
-            const __half2 p = __floats2half2_rn(acc[g * 32 + 2 * i], acc[g * 32 + 2 * i + 1]);
-            const uint32_t b2 = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
-                                ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
-            const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&b2));
-            packed[i] = *reinterpret_cast<const uint32_t*>(&yv);
+            for (int i4 = 0; i4 < 8; ++i4) {
+              float v[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * i4 + jj;
+                const float bj = ep_widen(__shfl_sync(0xffffffffu, blu, j), dt);
+                v[jj] = args.has_bias ? __fadd_rn(acc[g * 32 + j], bj) : acc[g * 32 + j];
+              }
+              if (row < M) {
+                if (args.y_vec && nc + 4 * i4 + 4 <= N) {
+                  *reinterpret_cast<float4*>(yr + 4 * i4) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                  for (int jj = 0; jj < 4; ++jj)
+                    if (nc + 4 * i4 + jj < N) yr[4 * i4 + jj] = v[jj];
+                }
+              }
+            }
+            continue;
+          }
+          uint32_t packed[16];
+          if constexpr (!GEN) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              // proj = RN16(acc) for two columns, then y = RN16(proj + b)
+              const __half2 p = __floats2half2_rn(acc[g * 32 + 2 * i], acc[g * 32 + 2 * i + 1]);
+              const uint32_t b2 = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
+                                  ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
+              const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&b2));
+              packed[i] = *reinterpret_cast<const uint32_t*>(&yv);
+            }
+          } else {
+            // head value t = RN_h(sum), then RN_h(t + b), then the steps
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              uint32_t t = ep_pack(acc[g * 32 + 2 * i], acc[g * 32 + 2 * i + 1], dt);
+              const float b0 = ep_widen(__shfl_sync(0xffffffffu, blu, 2 * i), dt);
+              const float b1 = ep_widen(__shfl_sync(0xffffffffu, blu, 2 * i + 1), dt);
+              if (args.has_bias) {
+                const float2 tv = ep_unpack(t, dt);
+                t = ep_pack(__fadd_rn(tv.x, b0), __fadd_rn(tv.y, b1), dt);
+              }
+              packed[i] = t;
+            }
+            const int row = m0 + q * 32 + lane;
+            for (int s = 0; s < args.num_steps; ++s) {
+              const int op = args.ep_op[s];
+              if (op == kEpAdd || op == kEpMul) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                  const uint4 rv = ep_load8(args.ep_ptr[s], args.ep_ld[s], row, M, nc + 8 * ch, N, args.ep_vec[s] != 0);
+                  const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                  for (int p2 = 0; p2 < 4; ++p2) {
+                    const float2 tv = ep_unpack(packed[4 * ch + p2], dt), r = ep_unpack(rw[p2], dt);
+                    packed[4 * ch + p2] = op == kEpAdd ? ep_pack(__fadd_rn(tv.x, r.x), __fadd_rn(tv.y, r.y), dt)
+                                                       : ep_pack(__fmul_rn(tv.x, r.x), __fmul_rn(tv.y, r.y), dt);
+                  }
+                }
+              } else {
+                uint32_t tmp[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tmp[i] = packed[i];
+                gemm_epi_activation16(tmp, op, dt);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) packed[i] = tmp[i];
+              }
+            }
           }
           if (args.tma_store) {
             if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it

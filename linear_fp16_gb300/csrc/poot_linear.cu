@@ -50,9 +50,9 @@ int cuda_fail(cudaError_t e) {
   return POOT_ERR_CUDA;
 }
 
-template <int MODE, int CL>
+template <int MODE, int CL, bool GEN = false>
 cudaError_t set_gemm_attrs() {
-  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout::DYN_BYTES);
 }
 
@@ -112,6 +112,10 @@ int device_state(int* dev_out, DeviceState** st_out) {
           (e = set_gemm_attrs<kLoadTma, 4>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadCpAsync4, 1>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadReg16, 1>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 1, true>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 2, true>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadCpAsync4, 1, true>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadReg16, 1, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<1, true>()) != cudaSuccess || (e = set_gemv_attrs<2, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<4, true>()) != cudaSuccess || (e = set_gemv_attrs<8, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<16, true>()) != cudaSuccess ||
@@ -221,14 +225,16 @@ bool variant_applicable(int v, const void* x, const void* w, int64_t M, int64_t 
   }
 }
 
-// Row-major [outer, inner] binary16 tensor, box [box_outer, box_inner].
+// Row-major [outer, inner] tensor of 2-byte elements (binary16, or bfloat16
+// when bf16), box [box_outer, box_inner].
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-               uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+               uint32_t box_outer, CUtensorMapSwizzle swizzle, bool bf16 = false) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+  const CUresult r = g_encode_tiled(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                    2, const_cast<void*>(base), dims,
                                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -313,9 +319,17 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, 
   return p;
 }
 
+// The widened contraction's epilogue, as checked by poot_contract.
+struct EpiConfig {
+  int dtype, out_f32, num_steps;
+  int op[kEpiMaxSteps];
+  const void* ptr[kEpiMaxSteps];
+  int64_t ld[kEpiMaxSteps];
+};
+
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
                 int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
-                cudaStream_t stream) {
+                cudaStream_t stream, const EpiConfig* epi = nullptr) {
   const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
                                   cluster_req, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
@@ -342,6 +356,22 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
   a.num_tiles = static_cast<int>(tiles);
   a.tma_store = (N % 8 == 0 && aligned(y, 16)) ? 1 : 0;
+  a.general = epi != nullptr ? 1 : 0;
+  a.dtype = epi != nullptr ? epi->dtype : POOT_DTYPE_F16;
+  a.out_f32 = (epi != nullptr && epi->out_f32) ? 1 : 0;
+  a.has_bias = (epi == nullptr || b != nullptr) ? 1 : 0;
+  a.y_vec = (N % 4 == 0 && aligned(y, 16)) ? 1 : 0;
+  a.y32 = a.out_f32 ? static_cast<float*>(y) : nullptr;
+  if (a.out_f32) a.tma_store = 0;
+  a.num_steps = epi != nullptr ? epi->num_steps : 0;
+  for (int s = 0; s < kEpiMaxSteps; ++s) {
+    const bool used = s < a.num_steps;
+    a.ep_op[s] = used ? epi->op[s] : 0;
+    a.ep_ptr[s] = used ? static_cast<const uint16_t*>(epi->ptr[s]) : nullptr;
+    a.ep_ld[s] = used ? epi->ld[s] : 0;
+    a.ep_vec[s] = (used && a.ep_ptr[s] != nullptr && aligned(a.ep_ptr[s], 16) && a.ep_ld[s] % 8 == 0) ? 1 : 0;
+  }
+  const bool bf16 = a.dtype == POOT_DTYPE_BF16;
   // Paired stages (see GemmArgs::paired) need an even ring and every chunk
   // (the tile's last one included) an even number of at least `stages` K
   // blocks: the fill that reuses a chunk's last pair then lies in the next
@@ -362,15 +392,44 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   std::memset(&tw, 0, sizeof(tw));
   std::memset(&ty, 0, sizeof(ty));
   if (variant == POOT_VARIANT_GEMM_TMA) {
-    if (!encode_2d(&tx, x, K, M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!encode_2d(&tx, x, K, M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                   bf16) ||
         !encode_2d(&tw, w, K, N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+                   CU_TENSOR_MAP_SWIZZLE_128B, bf16))
       return cuda_fail(cudaErrorInvalidValue);
   }
-  if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+  if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16))
     return cuda_fail(cudaErrorInvalidValue);
 
   cudaError_t e;
+  if (epi != nullptr) {
+    // the widened epilogue is compiled into its own instantiations (CTA
+    // pairs or single CTAs; clusters of four are not offered here)
+    if (plan.cluster == 4) return POOT_ERR_INVALID_ARG;
+    if (plan.cluster == 2) {
+      const int64_t pairs = st.sm_count / 2;
+      const int grid = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
+      e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 2, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                           Layout::DYN_BYTES, stream, 2u, tx, tw, ty, a);
+      return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+    }
+    const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
+    switch (variant) {
+      case POOT_VARIANT_GEMM_TMA:
+        e = launch(gemm_f16_tcgen05_kernel<kLoadTma, 1, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                   Layout::DYN_BYTES, stream, tx, tw, ty, a);
+        break;
+      case POOT_VARIANT_GEMM_CPASYNC:
+        e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1, true>, dim3(grid),
+                   dim3(gemm_threads(kLoadCpAsync4)), Layout::DYN_BYTES, stream, tx, tw, ty, a);
+        break;
+      default:
+        e = launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1, true>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
+                   Layout::DYN_BYTES, stream, tx, tw, ty, a);
+        break;
+    }
+    return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+  }
   if (plan.cluster == 4) {
     const int64_t clusters = st.max_clusters4;
     const int grid = 4 * static_cast<int>(tiles < clusters ? tiles : clusters);
@@ -467,6 +526,15 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
 
+// GEMM options shared by run() and contract().
+bool gemm_options_ok(const poot_linear_options& o) {
+  if (o.gemm_tile_n != 0 && (o.gemm_tile_n < 64 || o.gemm_tile_n > kGemmMaxBN || o.gemm_tile_n % 32 != 0))
+    return false;
+  if (o.gemm_group_m < 0) return false;
+  if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return false;
+  return o.gemm_cluster == 0 || o.gemm_cluster == 1 || o.gemm_cluster == 2 || o.gemm_cluster == 4;
+}
+
 int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
         const poot_linear_options& o, cudaStream_t stream) {
   int rc = validate(x, w, b, y, M, N, K);
@@ -476,12 +544,7 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
   if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_REG) return POOT_ERR_INVALID_ARG;
   if (gemv_wpr != 0 && gemv_wpr != 1 && gemv_wpr != 2 && gemv_wpr != 4 && gemv_wpr != 8)
     return POOT_ERR_INVALID_ARG;
-  if (o.gemm_tile_n != 0 && (o.gemm_tile_n < 64 || o.gemm_tile_n > kGemmMaxBN || o.gemm_tile_n % 32 != 0))
-    return POOT_ERR_INVALID_ARG;
-  if (o.gemm_group_m < 0) return POOT_ERR_INVALID_ARG;
-  if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return POOT_ERR_INVALID_ARG;
-  if (o.gemm_cluster != 0 && o.gemm_cluster != 1 && o.gemm_cluster != 2 && o.gemm_cluster != 4)
-    return POOT_ERR_INVALID_ARG;
+  if (!gemm_options_ok(o)) return POOT_ERR_INVALID_ARG;
   if (o.gemm_cluster > 1 && variant != POOT_VARIANT_AUTO && variant != POOT_VARIANT_GEMM_TMA)
     return POOT_ERR_INVALID_ARG;
   if (variant == POOT_VARIANT_AUTO) {
@@ -516,9 +579,77 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
   }
 }
 
+// The widened contraction: argument checks, GEMM variant, launch.
+int contract(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+             const poot_contraction_spec* spec, const poot_linear_options* opts, cudaStream_t stream) {
+  if (spec == nullptr) return POOT_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return POOT_ERR_INVALID_ARG;
+  if (spec->dtype != POOT_DTYPE_F16 && spec->dtype != POOT_DTYPE_BF16) return POOT_ERR_INVALID_ARG;
+  if (spec->num_steps < 0 || spec->num_steps > POOT_EPILOGUE_MAX_STEPS) return POOT_ERR_INVALID_ARG;
+  if (spec->out_f32 != 0 && spec->out_f32 != 1) return POOT_ERR_INVALID_ARG;
+  if (spec->out_f32 && spec->num_steps != 0) return POOT_ERR_INVALID_ARG;
+  EpiConfig epi;
+  std::memset(&epi, 0, sizeof(epi));
+  epi.dtype = spec->dtype;
+  epi.out_f32 = spec->out_f32;
+  epi.num_steps = spec->num_steps;
+  for (int s = 0; s < spec->num_steps; ++s) {
+    const poot_epilogue_step& st = spec->steps[s];
+    if (st.op < POOT_EP_ADD || st.op > POOT_EP_GELU_ERF) return POOT_ERR_INVALID_ARG;
+    epi.op[s] = st.op;
+    if (st.op == POOT_EP_ADD || st.op == POOT_EP_MUL) {
+      const int64_t ld = st.ld == 0 ? N : st.ld;
+      if (st.operand == nullptr || ld < N || ld > kMaxDim) return POOT_ERR_INVALID_ARG;
+      epi.ptr[s] = st.operand;
+      epi.ld[s] = ld;
+    }
+  }
+  poot_linear_options o;
+  std::memset(&o, 0, sizeof(o));
+  o.variant = POOT_VARIANT_AUTO;
+  if (opts != nullptr) o = *opts;
+  if (!gemm_options_ok(o) || o.gemm_cluster == 4) return POOT_ERR_INVALID_ARG;
+  if (o.variant != POOT_VARIANT_AUTO && o.variant != POOT_VARIANT_GEMM_TMA && o.variant != POOT_VARIANT_GEMM_CPASYNC &&
+      o.variant != POOT_VARIANT_GEMM_REG)
+    return POOT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return POOT_OK;
+  if (K == 0 || x == nullptr || w == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
+  if (!aligned(x, 2) || !aligned(w, 2) || (b != nullptr && !aligned(b, 2)) || !aligned(y, spec->out_f32 ? 4 : 2))
+    return POOT_ERR_MISALIGNED;
+  const int64_t ybytes = M * N * (spec->out_f32 ? 4 : 2);
+  if (overlaps(y, ybytes, x, M * K * 2) || overlaps(y, ybytes, w, N * K * 2) ||
+      (b != nullptr && overlaps(y, ybytes, b, N * 2)))
+    return POOT_ERR_INVALID_ARG;
+  for (int s = 0; s < epi.num_steps; ++s) {
+    if (epi.ptr[s] == nullptr) continue;
+    if (!aligned(epi.ptr[s], 2)) return POOT_ERR_MISALIGNED;
+    if (overlaps(y, ybytes, epi.ptr[s], ((M - 1) * epi.ld[s] + N) * 2)) return POOT_ERR_INVALID_ARG;
+  }
+  int variant = o.variant;
+  if (variant == POOT_VARIANT_AUTO) {
+    if (xw_tma_ok(x, w, K)) variant = POOT_VARIANT_GEMM_TMA;
+    else if (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) variant = POOT_VARIANT_GEMM_CPASYNC;
+    else variant = POOT_VARIANT_GEMM_REG;
+  } else if (!variant_applicable(variant, x, w, M, N, K)) {
+    return POOT_ERR_INVALID_ARG;
+  }
+  if (o.gemm_cluster == 2 && variant != POOT_VARIANT_GEMM_TMA) return POOT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  const int rc = device_state(&dev, &st);
+  if (rc != POOT_OK) return rc;
+  return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
+                     o.gemm_cluster, stream, &epi);
+}
+
 }  // namespace
 
 extern "C" {
+
+int poot_contract(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+                  const poot_contraction_spec* spec, const poot_linear_options* opts, poot_stream_t stream) {
+  return contract(x, w, b, y, M, N, K, spec, opts, reinterpret_cast<cudaStream_t>(stream));
+}
 
 int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
                     poot_stream_t stream) {

@@ -32,7 +32,7 @@ def test_library_builds_and_loads():
 
 def test_every_declared_symbol_is_exported_and_bound():
     names = declared_functions()
-    assert len(names) == 7, names
+    assert len(names) == 8, names
     lib = L.load_library()
     for n in names:
         assert hasattr(lib, n), n
@@ -170,3 +170,54 @@ def test_tensor_call_checks_types():
         L.linear(x, x, torch.zeros(2, dtype=torch.float16))  # CPU tensors are refused
     with pytest.raises(TypeError):
         L.linear(x.float(), x, torch.zeros(2, dtype=torch.float16))
+
+
+# ---- the widened contraction (poot_contract) ------------------------------------
+R = 0x5000_0000_0  # fake epilogue operand
+
+
+def _spec(dtype=L.DTYPE_F16, out_f32=0, steps=()):
+    sp = L.ContractionSpec()
+    sp.dtype, sp.out_f32, sp.num_steps = dtype, out_f32, len(steps)
+    for i, (op, ptr, ld) in enumerate(steps):
+        sp.steps[i].op, sp.steps[i].operand, sp.steps[i].ld = op, ptr, ld
+    return sp
+
+
+@pytest.mark.parametrize("spec,args,code", [
+    (_spec(dtype=2), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    (_spec(out_f32=2), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    (_spec(out_f32=1, steps=[(L.EP_SILU, 0, 0)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    (_spec(steps=[(9, 0, 0)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    (_spec(steps=[(L.EP_ADD, 0, 0)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),   # no operand
+    (_spec(steps=[(L.EP_MUL, R, 3)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),   # ld < N
+    (_spec(steps=[(L.EP_MUL, R + 1, 0)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    (_spec(steps=[(L.EP_ADD, Y + 8, 0)]), (X, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),  # overlaps y
+    (_spec(), (X, W, B, Y, 4, 4, 0), L.POOT_ERR_INVALID_ARG),                          # K == 0
+    (_spec(), (0, W, B, Y, 4, 4, 4), L.POOT_ERR_INVALID_ARG),
+    (_spec(), (X, W, B, Y + 1, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    (_spec(out_f32=1), (X, W, B, Y + 2, 4, 4, 4), L.POOT_ERR_MISALIGNED),             # float32 y
+    (_spec(), (X, W, B + 1, Y, 4, 4, 4), L.POOT_ERR_MISALIGNED),
+    (_spec(), (X, W, B, X + 8, 4, 4, 4), L.POOT_ERR_INVALID_ARG),                     # y overlaps x
+])
+def test_contract_argument_errors_before_any_cuda_call(spec, args, code):
+    assert L.poot_contract(*args, spec, None, 0) == code
+
+
+def test_contract_rejects_clusters_of_four_and_gemv_variants():
+    assert L.poot_contract(X, W, B, Y, 400, 64, 64, _spec(), L.options(gemm_cluster=4), 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(X, W, B, Y, 4, 64, 64, _spec(), L.options(L.VARIANT_GEMV), 0) == L.POOT_ERR_INVALID_ARG
+
+
+def test_contract_null_spec_and_empty_problems():
+    lib = L.load_library()
+    assert lib.poot_contract(X, W, B, Y, 4, 4, 4, None, None, 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(0, 0, 0, 0, 0, 5, 5, _spec(), None, 0) == L.POOT_OK
+
+
+def test_contract_bias_is_optional():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # passes every check and reaches the device query, which fails without a GPU
+    assert L.poot_contract(X, W, 0, Y, 4, 64, 64, _spec(), None, 0) == L.POOT_ERR_CUDA
