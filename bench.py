@@ -83,6 +83,8 @@ def parse_args():
     p.add_argument("--k-chunk", type=int, default=0, help="GEMM TMEM chunk along K (0 = automatic)")
     p.add_argument("--contract", default="", choices=[""] + sorted(CONTRACT_FORMS),
                    help="time a widened-contraction form (poot_contract) instead of the plain linear")
+    p.add_argument("--groups", type=int, default=1,
+                   help="with --contract: G groups of M/G rows, each with its own W (poot_contract_grouped)")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -533,13 +535,21 @@ def run_contract(args, rank, world, local):
     tdt = torch.bfloat16 if dt_name == "bf16" else torch.float16
     wl = synth.WORKLOADS[args.workload]
     M, N, K = wl.M, wl.N, wl.K
+    G = max(1, args.groups)
+    if M % G:
+        raise SystemExit(f"bench.py: M = {M} is not a multiple of --groups {G}")
     x_h, w_h, b_h = synth.workload_inputs(args.workload, seed_offset=0)
     x, w, b = (t.to(dev).to(tdt) for t in (x_h, w_h, b_h))
+    if G > 1:
+        # G experts: each its own copy of W and b, M/G rows of x
+        w = torch.cat([w] * G, dim=0).contiguous()
+        b = torch.cat([b] * G, dim=0).contiguous()
+    Mg = M // G
     g = torch.Generator(device="cpu").manual_seed(wl.seed + 77)
     n_ops = sum(1 for st in steps if not isinstance(st, str))
     ydt = torch.float32 if out_f32 else tdt
     ybytes = 4 if out_f32 else 2
-    working_set = 2 * (M * K + N * K + N) + ybytes * M * N + 2 * M * N * n_ops
+    working_set = 2 * (M * K + G * N * K + G * N) + ybytes * M * N + 2 * M * N * n_ops
     copies = 1 if working_set >= 3 * L2_BYTES else min(64, -(-3 * L2_BYTES // working_set))
     sets = []
     for c in range(copies):
@@ -564,8 +574,13 @@ def run_contract(args, rank, world, local):
 
     def step(i, sh):
         xs, ws, bs, y, _, spec = sets[i % copies]
-        rc = lib.poot_contract(xs.data_ptr(), ws.data_ptr(), bs.data_ptr() if bs is not None else None,
-                               y.data_ptr(), M, N, K, ctypes.byref(spec), ctypes.byref(opts), sh)
+        bp = bs.data_ptr() if bs is not None else None
+        if G > 1:
+            rc = lib.poot_contract_grouped(xs.data_ptr(), ws.data_ptr(), bp, y.data_ptr(), G, Mg, N, K,
+                                           ctypes.byref(spec), ctypes.byref(opts), sh)
+        else:
+            rc = lib.poot_contract(xs.data_ptr(), ws.data_ptr(), bp, y.data_ptr(), M, N, K, ctypes.byref(spec),
+                                   ctypes.byref(opts), sh)
         if rc != 0:
             raise RuntimeError(f"poot_contract: {L.poot_linear_status_string(rc)}")
 
@@ -606,13 +621,13 @@ def run_contract(args, rank, world, local):
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (step_ms * 1e-3) / 1e12
-    alg_bytes = 2 * (M * K + N * K + (N if with_bias else 0)) + ybytes * M * N + 2 * M * N * n_ops
+    alg_bytes = 2 * (M * K + G * N * K + (G * N if with_bias else 0)) + ybytes * M * N + 2 * M * N * n_ops
     line = {
         "metric": METRIC, "value": world * achieved, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dt_name, "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "N": N, "K": K, "dist": wl.dist, "seed": wl.seed,
-                   "accumulate": "f32", "contract": args.contract, "out": "f32" if out_f32 else dt_name,
+                   "accumulate": "f32", "contract": args.contract, "groups": G, "out": "f32" if out_f32 else dt_name,
                    "bias": with_bias, "steps": [st if isinstance(st, str) else st[0] for st in steps],
                    "l2": "inputs larger than L2" if copies == 1 else f"{copies} rotating copies",
                    "timing": "CUDA graph of the K steps, replayed between two events",

@@ -237,6 +237,22 @@ POOT_API int poot_contract(const void* x, const void* w, const void* b, void* y,
                            int64_t K, const poot_contraction_spec* spec, const poot_linear_options* opts,
                            poot_stream_t stream);
 
+/*
+ * Grouped contraction: G independent contractions in one launch, the
+ * GroupedDenseContraction row of the OpKind table ("ML compiler
+ * internals", section "The OpKind vocabulary": a [G*N, K] weight read in
+ * place as G blocks of N rows against a [G, M, K] activation).  For every
+ * group g:  y[g] = contraction(x[g], W[g*N .. g*N+N-1], b[g*N ..]) under
+ * `spec`, exactly as poot_contract computes it.
+ *   x [G, M, K], W [G*N, K], b [G*N] or NULL, y [G, M, N] (float32 when
+ *   spec->out_f32), step operands [G*M, ld] (row g*M + m belongs to group g).
+ * A batched contraction with one shared W is the plain call with M' = G*M.
+ * G >= 1 with G*M and G*N at most 2^31 - 1; other errors as poot_contract.
+ */
+POOT_API int poot_contract_grouped(const void* x, const void* w, const void* b, void* y, int64_t G, int64_t M,
+                                   int64_t N, int64_t K, const poot_contraction_spec* spec,
+                                   const poot_linear_options* opts, poot_stream_t stream);
+
 /* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
 POOT_API int poot_linear_version(void);
 

@@ -14,7 +14,7 @@ from .binding import (  # noqa: F401
     poot_linear_f16_ex, poot_linear_f16_variant, poot_linear_last_cuda_error,
     poot_linear_status_string, poot_linear_version, variant_for,
     ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,
-    EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract,
+    EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract, poot_contract_grouped,
 )
 
 __version__ = "0.1.0"

@@ -87,6 +87,8 @@ EXPORTS = {
     "poot_linear_version": (ctypes.c_int, []),
     "poot_contract": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.POINTER(ContractionSpec),
                                      ctypes.POINTER(Options), _VP]),
+    "poot_contract_grouped": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64,
+                                             ctypes.POINTER(ContractionSpec), ctypes.POINTER(Options), _VP]),
 }
 
 _lock = threading.Lock()
@@ -163,6 +165,13 @@ def poot_contract(x: int, w: int, b: int, y: int, M: int, N: int, K: int, spec, 
     return load_library().poot_contract(x, w, b or None, y, M, N, K, ctypes.byref(spec), ref, stream)
 
 
+def poot_contract_grouped(x: int, w: int, b: int, y: int, G: int, M: int, N: int, K: int, spec, opts,
+                          stream: int) -> int:
+    """G contractions: x [G,M,K], w [G*N,K], b [G*N] (or 0), y [G,M,N]."""
+    ref = ctypes.byref(opts) if opts is not None else None
+    return load_library().poot_contract_grouped(x, w, b or None, y, G, M, N, K, ctypes.byref(spec), ref, stream)
+
+
 status_string = poot_linear_status_string
 last_cuda_error = poot_linear_last_cuda_error
 
@@ -233,7 +242,9 @@ def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_ti
     """The widened contraction (include/poot_linear.h, poot_contract).
 
     x [M,K], w [N,K] and b [N] (or None) are float16 or bfloat16 CUDA
-    tensors of one dtype (the head dtype).  ``steps``: a sequence of
+    tensors of one dtype (the head dtype).  A 3-D x [G,M,K] with w [G*N,K]
+    and b [G*N] runs the grouped form (poot_contract_grouped); y is then
+    [G,M,N] and step operands [G,M,N].  ``steps``: a sequence of
     "silu", "gelu_tanh", "gelu_erf" or ("add" | "mul", r) with r an [M,N]
     tensor (row pitch from its stride) of the head dtype.  Returns y [M,N]:
     float32 with ``out_f32`` (no steps then), else the head dtype.
@@ -245,12 +256,17 @@ def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_ti
     for name, t in (("x", x), ("w", w)) + ((("b", b),) if b is not None else ()):
         if not isinstance(t, torch.Tensor) or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor of x's dtype")
-    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
-        raise ValueError(f"x [M,K] and w [N,K] expected, got {tuple(x.shape)} {tuple(w.shape)}")
-    M, K = x.shape
-    N = w.shape[0]
-    if b is not None and tuple(b.shape) != (N,):
-        raise ValueError(f"b must be [N], got {tuple(b.shape)}")
+    grouped = x.dim() == 3
+    if x.dim() not in (2, 3) or w.dim() != 2 or x.shape[-1] != w.shape[1]:
+        raise ValueError(f"x [M,K] or [G,M,K] and w [N,K] or [G*N,K] expected, got {tuple(x.shape)} "
+                         f"{tuple(w.shape)}")
+    G = x.shape[0] if grouped else 1
+    M, K = x.shape[-2], x.shape[-1]
+    if w.shape[0] % G != 0:
+        raise ValueError(f"w must hold G = {G} blocks of N rows, got {tuple(w.shape)}")
+    N = w.shape[0] // G
+    if b is not None and tuple(b.shape) != (G * N,):
+        raise ValueError(f"b must be [{'G*' if grouped else ''}N], got {tuple(b.shape)}")
     steps = list(steps)
     if len(steps) > EPILOGUE_MAX_STEPS:
         raise ValueError(f"at most {EPILOGUE_MAX_STEPS} epilogue steps")
@@ -265,21 +281,28 @@ def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_ti
         spec.steps[i].op = EP_CODES[name]
         if name in ("add", "mul"):
             r = operand
-            if (not isinstance(r, torch.Tensor) or r.dtype != dt or not r.is_cuda or r.dim() != 2
-                    or tuple(r.shape) != (M, N) or r.stride(1) != 1):
-                raise ValueError(f"step {name}: an [M,N] CUDA tensor of x's dtype with unit column stride")
+            if (not isinstance(r, torch.Tensor) or r.dtype != dt or not r.is_cuda or r.dim() != x.dim()
+                    or tuple(r.shape) != tuple(x.shape[:-1]) + (N,) or r.stride(-1) != 1
+                    or (grouped and r.stride(0) != M * r.stride(1))):
+                raise ValueError(f"step {name}: a CUDA tensor of x's dtype shaped like y, unit column "
+                                 "stride (groups stacked by rows)")
             spec.steps[i].operand = r.data_ptr()
-            spec.steps[i].ld = r.stride(0)
+            spec.steps[i].ld = r.stride(-2)
     ydt = torch.float32 if out_f32 else dt
+    yshape = tuple(x.shape[:-1]) + (N,)
     if out is None:
-        out = torch.empty((M, N), dtype=ydt, device=x.device)
-    elif out.dtype != ydt or tuple(out.shape) != (M, N) or not out.is_contiguous():
-        raise ValueError(f"out must be a contiguous [M, N] {ydt} tensor")
+        out = torch.empty(yshape, dtype=ydt, device=x.device)
+    elif out.dtype != ydt or tuple(out.shape) != yshape or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {yshape} {ydt} tensor")
+    opts = options(variant, 0, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster)
+    bp = b.data_ptr() if b is not None else 0
     with torch.cuda.device(x.device):
         s = torch.cuda.current_stream(x.device) if stream is None else stream
-        rc = poot_contract(x.data_ptr(), w.data_ptr(), b.data_ptr() if b is not None else 0, out.data_ptr(),
-                           M, N, K, spec, options(variant, 0, gemm_tile_n, gemm_group_m, gemm_k_chunk,
-                                                  gemm_cluster), s.cuda_stream)
+        if grouped:
+            rc = poot_contract_grouped(x.data_ptr(), w.data_ptr(), bp, out.data_ptr(), G, M, N, K, spec, opts,
+                                       s.cuda_stream)
+        else:
+            rc = poot_contract(x.data_ptr(), w.data_ptr(), bp, out.data_ptr(), M, N, K, spec, opts, s.cuda_stream)
     if rc != POOT_OK:
-        raise PootLinearError(rc, "poot_contract")
+        raise PootLinearError(rc, "poot_contract_grouped" if grouped else "poot_contract")
     return out

@@ -70,6 +70,11 @@ struct GemmArgs {
   const uint16_t* ep_ptr[kEpiMaxSteps];
   long long ep_ld[kEpiMaxSteps];
   float* y32;
+  // grouped contraction (GEN only): tile t belongs to group t / tiles_per_group;
+  // x is [groups*M, K], W is [groups*N, K], y [groups, M, N], b [groups*N],
+  // step operands [groups*M, ld]
+  int groups;
+  int tiles_per_group;
 };
 
 // Activation step over the 16 packed pairs of one 32-column box (kept out of
@@ -261,6 +266,17 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const int chunk_kb = args.chunk_kb;
   const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
 
+  // tile t -> (group, M block, N block)
+  auto tile_decode = [&](int t, int& g, int& mb, int& nb) {
+    int tl = t;
+    g = 0;
+    if constexpr (GEN) {
+      g = t / args.tiles_per_group;
+      tl = t - g * args.tiles_per_group;
+    }
+    gemm_tile_coords(tl, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+  };
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -334,9 +350,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int step = paired ? 2 : 1;
         int ck = 0, ch = 0;
         for (int t = unit; t < args.num_tiles && ok; t += units) {
-          int mb, nb;
-          gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+          int g, mb, nb;
+          tile_decode(t, g, mb, nb);
           if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;  // this pair's N tile
+          // rows of this group in the flattened x [groups*M, K] and W [groups*N, K]
+          // (a tile that overhangs its group reads rows of the next one; they
+          // only reach output rows or columns that are never stored)
+          const int xrow0 = g * args.M, wrow0 = g * args.N;
           for (int kb = 0; kb < num_kb; kb += step) {
             const uint32_t eb = paired ? bar_empty(stage >> 1) : bar_empty(stage);
             if (paired && ck == STAGES - 2 && ch > 0) {
@@ -358,7 +378,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 // both CTAs' bytes complete on the even CTA's barrier
                 const uint32_t fb0 = map_to_cta(fb, lead_rank);
                 if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
-                const int arow = mb * tile_rows + (int)rank * kGemmBM;
+                const int arow = xrow0 + mb * tile_rows + (int)rank * kGemmBM;
                 if constexpr (CL == 4) {
                   // half of the x tile, into this CTA and its counterpart in the other pair
                   const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
@@ -367,11 +387,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 } else {
                   tma_load_2d_pair(stage_a(st), &tm_x, fb0, kc, arow);
                 }
-                tma_load_2d_pair(stage_b(st), &tm_w, fb0, kc, nb * BN + (int)rank * (BN / 2));
+                tma_load_2d_pair(stage_b(st), &tm_w, fb0, kc, wrow0 + nb * BN + (int)rank * (BN / 2));
               } else {
                 mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-                tma_load_2d(stage_a(st), &tm_x, fb, kc, mb * kGemmBM);
-                tma_load_2d(stage_b(st), &tm_w, fb, kc, nb * BN);
+                tma_load_2d(stage_a(st), &tm_x, fb, kc, xrow0 + mb * kGemmBM);
+                tma_load_2d(stage_b(st), &tm_w, fb, kc, wrow0 + nb * BN);
               }
             }
             if (ck + step >= chunk_kb || kb + step >= num_kb) { ck = 0; ++ch; } else { ck += step; }
@@ -406,17 +426,19 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       int filled = 0;                 // fills issued (saturates at LAG)
       bool ok = true;
       for (int t = unit; t < args.num_tiles && ok; t += units) {
-        int mb, nb;
-        gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+        int g, mb, nb;
+        tile_decode(t, g, mb, nb);
+        const __half* xg = args.x + (size_t)g * args.M * args.K;
+        const __half* wg = args.w + (size_t)g * args.N * args.K;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (MODE == kLoadCpAsync4) {
             if (w8) {
-              gemm_copy_rows_cp<8>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
-              gemm_copy_rows_cp<8>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<8>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<8>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
             } else {
-              gemm_copy_rows_cp<4>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
-              gemm_copy_rows_cp<4>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<4>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<4>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
             }
             cp_async_commit();
             if (filled == LAG) {
@@ -428,9 +450,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               ++filled;
             }
           } else {
-            gemm_copy_tile<MODE>(stage_a(stage), args.x, kGemmBM, mb * kGemmBM, args.M, args.K,
-                                 kb * kGemmBK, pt);
-            gemm_copy_tile<MODE>(stage_b(stage), args.w, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
+            gemm_copy_tile<MODE>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, pt);
+            gemm_copy_tile<MODE>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
             fence_proxy_async_smem();
             mbar_arrive(bar_full(stage));
           }
@@ -560,8 +581,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     const int M = args.M, N = args.N;
     bool ok = true;
     for (int t = unit; t < args.num_tiles && ok; t += units) {
-      int mb, nb;
-      gemm_tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      int grp, mb, nb;
+      tile_decode(t, grp, mb, nb);
       if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;
       const int m0 = mb * tile_rows + (int)rank * kGemmBM, n0 = nb * BN;
       // pull this warp's bias values into L1 now, so that the final epilogue
@@ -569,7 +590,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         const int col = n0 + col0 + g * 32 + lane;
-        if ((!GEN || args.has_bias) && g < ngroups && col < N) prefetch_l1(args.b + col);
+        if ((!GEN || args.has_bias) && g < ngroups && col < N) prefetch_l1(args.b + (size_t)grp * N + col);
       }
       float acc[kGemmHalfCols];
 #pragma unroll
@@ -602,11 +623,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       if (!ok) break;
       // final epilogue of this tile from registers; lane l of box g holds
       // b[n0 + col0 + 32g + l], all boxes loaded together
+      // this tile's group: its bias and output (step operands below)
+      const __half* bg = args.b + (size_t)grp * N;
+      __half* yg = args.y + (size_t)grp * M * N;
       unsigned short bias16[kGemmHalfCols / 32];
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         const int col = n0 + col0 + g * 32 + lane;
-        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(args.b[col])
+        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(bg[col])
                                                                          : (unsigned short)0;
       }
 #pragma unroll
@@ -620,7 +644,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             // FP32 output: the sum (+ b rounded once in FP32); lane = row,
             // its 32 consecutive columns stored directly
             const int row = m0 + q * 32 + lane;
-            float* yr = args.y32 + (size_t)(row < M ? row : 0) * N + nc;
+            float* yr = args.y32 + ((size_t)grp * M + (row < M ? row : 0)) * N + nc;
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
               float v[4];
@@ -672,7 +696,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               if (op == kEpAdd || op == kEpMul) {
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                  const uint4 rv = ep_load8(args.ep_ptr[s], args.ep_ld[s], row, M, nc + 8 * ch, N, args.ep_vec[s] != 0);
+                  const uint4 rv = ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s], row, M,
+                                            nc + 8 * ch, N, args.ep_vec[s] != 0);
                   const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
                   for (int p2 = 0; p2 < 4; ++p2) {
@@ -707,7 +732,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc, m0 + q * 32);
+              // the widened kernels store through a 3-D map [groups][M][N]
+              if constexpr (GEN) tma_store_3d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc, m0 + q * 32, grp);
+              else tma_store_2d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc, m0 + q * 32);
               bulk_commit_group();
             }
           } else {
@@ -719,7 +746,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               const int row = m0 + q * 32 + rr;
               if (row < M && col < N) {
                 const int pos = (lane >> 3) ^ ((rr >> 1) & 3);
-                args.y[(size_t)row * N + col] =
+                yg[(size_t)row * N + col] =
                     *reinterpret_cast<const __half*>(box + rr * 64 + pos * 16 + (lane & 7) * 2);
               }
             }

@@ -240,6 +240,21 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+// [slabs][outer][inner] tensor of 2-byte elements, box [1][box_outer][box_inner]
+// (each box stays inside one slab: stores clip at `outer` per slab).
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t slabs,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle, bool bf16) {
+  const cuuint64_t dims[3] = {inner, outer, slabs};
+  const cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode_tiled(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                    3, const_cast<void*>(base), dims, strides, box, estr,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct GemmPlan {
   int bn, stages, group_m, chunk_kb;
   int cluster;  // 1: single CTAs; 2: CTA pairs (2-SM MMA); 4: two pairs sharing x
@@ -329,7 +344,7 @@ struct EpiConfig {
 
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
                 int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
-                cudaStream_t stream, const EpiConfig* epi = nullptr) {
+                cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1) {
   const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
                                   cluster_req, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
@@ -352,9 +367,12 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
   if (plan.cluster == 4) a.num_n_blocks = (a.num_n_blocks + 1) / 2;  // tile pairs along N
   a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
-  const int64_t tiles = int64_t(a.num_m_blocks) * a.num_n_blocks;
+  const int64_t tiles_per_group = int64_t(a.num_m_blocks) * a.num_n_blocks;
+  const int64_t tiles = tiles_per_group * G;
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
   a.num_tiles = static_cast<int>(tiles);
+  a.groups = static_cast<int>(G);
+  a.tiles_per_group = static_cast<int>(tiles_per_group);
   a.tma_store = (N % 8 == 0 && aligned(y, 16)) ? 1 : 0;
   a.general = epi != nullptr ? 1 : 0;
   a.dtype = epi != nullptr ? epi->dtype : POOT_DTYPE_F16;
@@ -392,14 +410,20 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   std::memset(&tw, 0, sizeof(tw));
   std::memset(&ty, 0, sizeof(ty));
   if (variant == POOT_VARIANT_GEMM_TMA) {
-    if (!encode_2d(&tx, x, K, M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B,
-                   bf16) ||
-        !encode_2d(&tw, w, K, N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
+    // x and W of all groups as one flattened [G*M, K] and [G*N, K] tensor
+    if (!encode_2d(&tx, x, K, G * M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B, bf16) ||
+        !encode_2d(&tw, w, K, G * N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
                    CU_TENSOR_MAP_SWIZZLE_128B, bf16))
       return cuda_fail(cudaErrorInvalidValue);
   }
-  if (a.tma_store && !encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16))
-    return cuda_fail(cudaErrorInvalidValue);
+  if (a.tma_store) {
+    // the widened kernels store through [G][M][N] so that boxes clip at each
+    // group's M; the plain kernels through [M][N]
+    const bool ok = epi != nullptr ? encode_3d(&ty, y, N, M, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16)
+                                   : encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16);
+    if (!ok) return cuda_fail(cudaErrorInvalidValue);
+  }
 
   cudaError_t e;
   if (epi != nullptr) {
@@ -579,11 +603,13 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
   }
 }
 
-// The widened contraction: argument checks, GEMM variant, launch.
-int contract(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+// The widened contraction (G groups; G = 1 for poot_contract): argument
+// checks, GEMM variant, launch.
+int contract(const void* x, const void* w, const void* b, void* y, int64_t G, int64_t M, int64_t N, int64_t K,
              const poot_contraction_spec* spec, const poot_linear_options* opts, cudaStream_t stream) {
   if (spec == nullptr) return POOT_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return POOT_ERR_INVALID_ARG;
+  if (G < 1 || G > kMaxDim || G * M > kMaxDim || G * N > kMaxDim) return POOT_ERR_INVALID_ARG;
   if (spec->dtype != POOT_DTYPE_F16 && spec->dtype != POOT_DTYPE_BF16) return POOT_ERR_INVALID_ARG;
   if (spec->num_steps < 0 || spec->num_steps > POOT_EPILOGUE_MAX_STEPS) return POOT_ERR_INVALID_ARG;
   if (spec->out_f32 != 0 && spec->out_f32 != 1) return POOT_ERR_INVALID_ARG;
@@ -616,14 +642,14 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t M, in
   if (K == 0 || x == nullptr || w == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
   if (!aligned(x, 2) || !aligned(w, 2) || (b != nullptr && !aligned(b, 2)) || !aligned(y, spec->out_f32 ? 4 : 2))
     return POOT_ERR_MISALIGNED;
-  const int64_t ybytes = M * N * (spec->out_f32 ? 4 : 2);
-  if (overlaps(y, ybytes, x, M * K * 2) || overlaps(y, ybytes, w, N * K * 2) ||
-      (b != nullptr && overlaps(y, ybytes, b, N * 2)))
+  const int64_t ybytes = G * M * N * (spec->out_f32 ? 4 : 2);
+  if (overlaps(y, ybytes, x, G * M * K * 2) || overlaps(y, ybytes, w, G * N * K * 2) ||
+      (b != nullptr && overlaps(y, ybytes, b, G * N * 2)))
     return POOT_ERR_INVALID_ARG;
   for (int s = 0; s < epi.num_steps; ++s) {
     if (epi.ptr[s] == nullptr) continue;
     if (!aligned(epi.ptr[s], 2)) return POOT_ERR_MISALIGNED;
-    if (overlaps(y, ybytes, epi.ptr[s], ((M - 1) * epi.ld[s] + N) * 2)) return POOT_ERR_INVALID_ARG;
+    if (overlaps(y, ybytes, epi.ptr[s], ((G * M - 1) * epi.ld[s] + N) * 2)) return POOT_ERR_INVALID_ARG;
   }
   int variant = o.variant;
   if (variant == POOT_VARIANT_AUTO) {
@@ -639,7 +665,7 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t M, in
   const int rc = device_state(&dev, &st);
   if (rc != POOT_OK) return rc;
   return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
-                     o.gemm_cluster, stream, &epi);
+                     o.gemm_cluster, stream, &epi, G);
 }
 
 }  // namespace
@@ -648,7 +674,13 @@ extern "C" {
 
 int poot_contract(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
                   const poot_contraction_spec* spec, const poot_linear_options* opts, poot_stream_t stream) {
-  return contract(x, w, b, y, M, N, K, spec, opts, reinterpret_cast<cudaStream_t>(stream));
+  return contract(x, w, b, y, 1, M, N, K, spec, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_contract_grouped(const void* x, const void* w, const void* b, void* y, int64_t G, int64_t M, int64_t N,
+                          int64_t K, const poot_contraction_spec* spec, const poot_linear_options* opts,
+                          poot_stream_t stream) {
+  return contract(x, w, b, y, G, M, N, K, spec, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,

@@ -278,3 +278,26 @@ def bf16_to_f32(h) -> np.ndarray:
     out = np.empty(h.shape, dtype=np.float32)
     _lib().oracle_bf16_to_f32_array(_ptr(h, ctypes.c_uint16), _ptr(out, ctypes.c_float), h.size)
     return out
+
+
+def contraction_grouped(x, w, b=None, *, dtype: str = "f16", out_f32: bool = False, steps=(),
+                        nthreads: int | None = None):
+    """G independent contractions ("ML compiler internals", the
+    GroupedDenseContraction row): x [G,M,K], w [G*N,K] read as G blocks of
+    N rows, b [G*N] or None, step operands [G,M,N]; y [G,M,N].  Each group
+    is ``contraction`` of its own blocks."""
+    x = _u16any(x)
+    if x.ndim != 3:
+        raise ValueError("x [G,M,K] expected")
+    G = x.shape[0]
+    w = _u16any(w)
+    if w.shape[0] % G:
+        raise ValueError("w must hold G blocks of N rows")
+    N = w.shape[0] // G
+    outs = []
+    for g in range(G):
+        st = [s if isinstance(s, str) else (s[0], _u16any(s[1])[g]) for s in steps]
+        bg = None if b is None else _u16any(b)[g * N:(g + 1) * N]
+        outs.append(contraction(x[g], w[g * N:(g + 1) * N], bg, dtype=dtype, out_f32=out_f32, steps=st,
+                                nthreads=nthreads))
+    return np.stack(outs)

@@ -32,7 +32,7 @@ def test_library_builds_and_loads():
 
 def test_every_declared_symbol_is_exported_and_bound():
     names = declared_functions()
-    assert len(names) == 8, names
+    assert len(names) == 9, names
     lib = L.load_library()
     for n in names:
         assert hasattr(lib, n), n
@@ -221,3 +221,13 @@ def test_contract_bias_is_optional():
         pytest.skip("a GPU is present")
     # passes every check and reaches the device query, which fails without a GPU
     assert L.poot_contract(X, W, 0, Y, 4, 64, 64, _spec(), None, 0) == L.POOT_ERR_CUDA
+
+
+def test_grouped_argument_errors():
+    sp = _spec()
+    assert L.poot_contract_grouped(X, W, B, Y, 0, 4, 4, 4, sp, None, 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract_grouped(X, W, B, Y, 1 << 20, 1 << 12, 4, 4, sp, None, 0) == L.POOT_ERR_INVALID_ARG
+    # y of 3 groups runs into W when the groups are counted
+    assert L.poot_contract_grouped(X, W, B, W - 3 * 4 * 4 * 2 + 2, 3, 4, 4, 4, sp, None, 0) == \
+        L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract_grouped(0, 0, 0, 0, 3, 0, 4, 4, sp, None, 0) == L.POOT_OK

@@ -300,3 +300,64 @@ def test_contract_is_deterministic():
     a = _gpu(x, w, b, steps=["gelu_erf", ("mul", r)])
     c = _gpu(x, w, b, steps=["gelu_erf", ("mul", r)])
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+# ---- grouped contraction ----------------------------------------------------------
+def _grouped_inputs(G, M, N, K, dist, seed, dt):
+    x, w, b = _inputs(G * M, G * N, K, dist, seed, dt)
+    return x.reshape(G, M, K), w, b
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("G,M,N,K,pair", [
+    (4, 300, 264, 256, 0),      # M not a multiple of 128 or 256: tiles overhang their group
+    (3, 129, 72, 200, 1),       # single CTAs, ragged N
+    (8, 64, 520, 512, 0),       # many small groups
+    (2, 1000, 900, 770, 0),     # K % 8 != 0: the copy producers
+    (5, 256, 256, 128, 2),      # CTA pairs, groups of exactly one pair tile
+])
+def test_grouped_exact(dt, G, M, N, K, pair):
+    x, w, b = _grouped_inputs(G, M, N, K, "smallint", 400 + G + M, dt)
+    x = x / 4
+    r = _operand(G * M, N, "smallint", 401, dt).reshape(G, M, N)
+    steps = [("mul", r), ("add", r)]
+    y = _gpu(x, w, b, steps=steps, gemm_cluster=pair)
+    assert tuple(y.shape) == (G, M, N)
+    want = oracle.contraction_grouped(_bits(x.reshape(G, M, K)), _bits(w), _bits(b), dtype=dt,
+                                      steps=[(s[0], _bits(s[1])) for s in steps])
+    assert np.array_equal(_bits(y), want)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_grouped_activation_and_f32(dt):
+    G, M, N, K = 3, 200, 300, 512
+    x, w, b = _grouped_inputs(G, M, N, K, "normal", 410, dt)
+    steps = ["gelu_erf"]
+    y = _gpu(x, w, b, steps=steps)
+    for g in range(G):
+        _check_head(x[g], w[g * N:(g + 1) * N], b[g * N:(g + 1) * N], steps, y[g], dt, exact_sums=False)
+    yf = _gpu(x, w, None, out_f32=True)
+    for g in range(G):
+        _check_f32(x[g], w[g * N:(g + 1) * N], None, yf[g], dt, exact_sums=False)
+
+
+def test_grouped_with_one_group_equals_the_plain_form():
+    x, w, b = _inputs(700, 520, 320, "normal", 420, "f16")
+    a = _gpu(x, w, b, steps=["silu"])
+    g1 = _gpu(x.reshape(1, 700, 320), w, b, steps=["silu"])
+    assert torch.equal(a.view(torch.int16), g1[0].view(torch.int16))
+
+
+def test_grouped_leaves_other_groups_rows_alone():
+    # every group's y block is written exactly; a guard row after the last
+    # group (part of the same allocation) is never touched
+    G, M, N, K = 3, 131, 264, 128
+    x, w, b = _grouped_inputs(G, M, N, K, "smallint", 430, "f16")
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    buf = torch.full((G * M + 1, N), 12345.0, dtype=torch.float16, device=DEV)
+    y = buf[:G * M].view(G, M, N)
+    L.contract(xd, wd, bd, out=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[G * M] == 12345.0)
+    want = oracle.contraction_grouped(_bits(x), _bits(w), _bits(b))
+    assert np.array_equal(_bits(y), want)

@@ -270,3 +270,22 @@ def test_unmutated_widened_oracle_passes_its_pins():
 @pytest.mark.parametrize("mutation", sorted(NEW_MUTATIONS))
 def test_widened_oracle_planted_mistake_is_caught(mutation):
     assert not _new_pins_pass(mutation), NEW_MUTATIONS[mutation]
+
+
+# ---- grouped ----------------------------------------------------------------------
+def test_grouped_is_the_diagonal_of_one_contraction():
+    # all groups' rows against all groups' W blocks in one contraction: block
+    # (g, g) of the result is group g of the grouped contraction
+    rng = np.random.default_rng(22)
+    G, M, N, K = 3, 5, 4, 24
+    x = rng.standard_normal((G, M, K)).astype(np.float16)
+    w = rng.standard_normal((G * N, K)).astype(np.float16)
+    b = rng.standard_normal(G * N).astype(np.float16)
+    r = rng.standard_normal((G, M, N)).astype(np.float16)
+    grouped = oracle.contraction_grouped(x, w, b, steps=[("mul", r), "silu"])
+    full_r = np.zeros((G * M, G * N), dtype=np.float16)
+    for g in range(G):
+        full_r[g * M:(g + 1) * M, g * N:(g + 1) * N] = r[g]
+    full = oracle.contraction(x.reshape(G * M, K), w, b, steps=[("mul", full_r), "silu"])
+    for g in range(G):
+        assert np.array_equal(grouped[g], full[g * M:(g + 1) * M, g * N:(g + 1) * N])
