@@ -272,8 +272,12 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
 // that permutation these registers are exactly the A (W) and B (x^T)
 // fragments of two m16n8k16 MMAs, and no shuffles are needed.  D[n][m]
 // accumulates y^T; warps meet in shared memory in a fixed order.
-constexpr int kGemvMmaWarps = 8;
-constexpr int kGemvMmaThreads = kGemvMmaWarps * 32;
+// WARPS (8 or 16) split K: with few 16-row tiles per SM (N/16 < 2 SMs) 16
+// warps keep twice the W bytes of a tile in flight (GB300, 8 x 4096 x 4096:
+// 8.5 us against 10.1 us with 8); with many tiles 8 warps are better
+// (8 x 14336 x 4096: 23.6 us against 27.5 us).
+constexpr int kGemvMmaWarpsFew = 16;
+constexpr int kGemvMmaWarpsMany = 8;
 
 __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                   uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -285,9 +289,9 @@ __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, ui
 }
 
 // NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16)
-template <int NT>
-__global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const GemvArgs a) {
-  __shared__ float red[kGemvMmaWarps][32][4 * NT];
+template <int NT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs a) {
+  __shared__ float red[WARPS][32][4 * NT];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const Gem
   const int K = a.K, N = a.N, M = a.M;
   const int nA = n0 + g, nB = n0 + g + 8;
   // this warp's K slice, a multiple of 32
-  const int slice = ((K + kGemvMmaWarps * 32 - 1) / (kGemvMmaWarps * 32)) * 32;
+  const int slice = ((K + WARPS * 32 - 1) / (WARPS * 32)) * 32;
   const int k_begin = min(K, warp * slice);
   const int k_end = min(K, k_begin + slice);
   const __half* __restrict__ wa = a.w + (size_t)(nA < N ? nA : 0) * K;
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kGemvMmaThreads) gemv_f16_mma_kernel(const Gem
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float s = red[0][lane][4 * q + i];
-      for (int wi = 1; wi < kGemvMmaWarps; ++wi) s += red[wi][lane][4 * q + i];
+      for (int wi = 1; wi < WARPS; ++wi) s += red[wi][lane][4 * q + i];
       // D[n][m]: i = 0, 1 -> (n = nA, m = 2t + i); i = 2, 3 -> (n = nB, m = 2t + i - 2)
       const int m = 8 * q + 2 * t + (i & 1);
       const int n = (i < 2) ? nA : nB;

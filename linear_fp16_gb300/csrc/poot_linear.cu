@@ -536,12 +536,18 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
     else
       e = launch(gemv_f16_rows_kernel<2>, rgrid, dim3(kGemvRowThreads), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV && wpr_req == 0) {
-    // 3 <= M <= 16 on the tensor cores, 16 rows of W per block
-    const dim3 mgrid(static_cast<unsigned>((N + 15) / 16));
+    // 3 <= M <= 16 on the tensor cores, 16 rows of W per block; 16 warps
+    // along K when there are fewer than two such blocks per SM
+    const int64_t tiles = (N + 15) / 16;
+    const dim3 mgrid(static_cast<unsigned>(tiles));
+    const bool few = tiles < 2 * int64_t(st.sm_count);
+    constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
     if (M <= 8)
-      e = launch(gemv_f16_mma_kernel<1>, mgrid, dim3(kGemvMmaThreads), 0, stream, a);
+      e = few ? launch(gemv_f16_mma_kernel<1, WF>, mgrid, dim3(WF * 32), 0, stream, a)
+              : launch(gemv_f16_mma_kernel<1, WM>, mgrid, dim3(WM * 32), 0, stream, a);
     else
-      e = launch(gemv_f16_mma_kernel<2>, mgrid, dim3(kGemvMmaThreads), 0, stream, a);
+      e = few ? launch(gemv_f16_mma_kernel<2, WF>, mgrid, dim3(WF * 32), 0, stream, a)
+              : launch(gemv_f16_mma_kernel<2, WM>, mgrid, dim3(WM * 32), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV) {
     e = launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
   } else {
