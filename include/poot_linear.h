@@ -96,7 +96,10 @@ enum {
  * stream: the work is queued on it; the call does not synchronise.
  * Ownership: the caller owns all four buffers.  x, w and b are only read;
  *   every element of y is written.  y must not overlap x, w or b.  The
- *   library allocates nothing per call.
+ *   library allocates nothing per call, except that a split-K plan (small
+ *   M, long K; see gemm_split_k) takes its FP32 workspace from a buffer the
+ *   library keeps per device and stream, allocating or growing it on first
+ *   need (a graph-owned block under stream capture).
  * Errors: argument errors are found before any CUDA call and nothing is
  *   queued.  Launch failures return POOT_ERR_CUDA.  Faults inside a kernel
  *   surface at the caller's next synchronisation, as for any CUDA kernel;
@@ -129,6 +132,23 @@ typedef struct poot_linear_options {
                                 tiles (2-SM MMA); 4 = two such pairs on
                                 neighbouring N tiles sharing the x tile.
                                 2 and 4 need the GEMM_TMA variant */
+    int gemm_split_k;        /* 0 = automatic; 1 = never; S in [2, 16] = cut
+                                the K range into S ranges of whole 64-element
+                                blocks (S must divide ceil(K / 64)), each
+                                summed by its own tiles into an FP32
+                                workspace, then added in range order by a
+                                second kernel that applies the epilogue.
+                                The workspace (S * M * N * 4 bytes) belongs to
+                                the library: one per device and stream, kept
+                                for the life of the process; under stream
+                                capture, a graph-owned allocation freed on
+                                the stream after the second kernel.  Not with
+                                gemm_cluster 4, nor with grouped contractions.
+                                Automatic splitting happens when the output
+                                tiles fill less than half of the SMs and K is
+                                at least 1024; when no workspace can be had,
+                                an automatic split falls back to none and a
+                                requested one returns POOT_ERR_CUDA */
 } poot_linear_options;
 
 /*
@@ -227,7 +247,8 @@ typedef struct poot_contraction_spec {
  * Runs on the tcgen05 GEMM for every M (the GEMV kernels serve only
  * poot_linear_f16).  `opts` may be NULL; its GEMV fields and variants are
  * ignored except the GEMM ones.  Asynchronous; the caller owns every
- * buffer; the library allocates nothing.
+ * buffer; the library allocates nothing except the split-K workspace
+ * described under poot_linear_f16 (never for the grouped form).
  * Errors: POOT_ERR_INVALID_ARG for a NULL spec, x, w or y, K == 0, a bad
  * dtype, step code, step count, NULL operand or ld < N, steps with out_f32,
  * or y overlapping x, W, b or an operand; POOT_ERR_MISALIGNED for a pointer

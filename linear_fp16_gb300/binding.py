@@ -54,12 +54,15 @@ class Options(ctypes.Structure):
     """struct poot_linear_options (include/poot_linear.h)."""
     _fields_ = [("variant", ctypes.c_int), ("gemv_warps_per_row", ctypes.c_int),
                 ("gemm_tile_n", ctypes.c_int), ("gemm_group_m", ctypes.c_int),
-                ("gemm_k_chunk", ctypes.c_int), ("gemm_cluster", ctypes.c_int)]
+                ("gemm_k_chunk", ctypes.c_int), ("gemm_cluster", ctypes.c_int),
+                ("gemm_split_k", ctypes.c_int)]
 
 
 def options(variant: int = -1, gemv_warps_per_row: int = 0, gemm_tile_n: int = 0,
-            gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0) -> Options:
-    return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster)
+            gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0,
+            gemm_split_k: int = 0) -> Options:
+    return Options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster,
+                   gemm_split_k)
 
 
 class EpilogueStep(ctypes.Structure):
@@ -193,7 +196,7 @@ def _check(t, name, ndim):
 
 def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row: int = 0,
            gemm_tile_n: int = 0, gemm_group_m: int = 0, gemm_k_chunk: int = 0,
-           gemm_cluster: int = 0, stream=None):
+           gemm_cluster: int = 0, gemm_split_k: int = 0, stream=None):
     """y = FP16(x . W^T) + b with x [M,K], w [N,K], b [N] fp16 CUDA tensors.
 
     Runs on ``stream`` (default: the current torch stream of x's device) and
@@ -221,7 +224,7 @@ def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row
         s = torch.cuda.current_stream(dev) if stream is None else stream
         rc = poot_linear_f16_ex(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
                                 options(variant, gemv_warps_per_row, gemm_tile_n, gemm_group_m,
-                                        gemm_k_chunk, gemm_cluster),
+                                        gemm_k_chunk, gemm_cluster, gemm_split_k),
                                 s.cuda_stream)
     if rc != POOT_OK:
         raise PootLinearError(rc, "poot_linear_f16")
@@ -237,8 +240,8 @@ def variant_for(x, w, b, y) -> int:
 
 # ---- tensor-level widened contraction ------------------------------------
 def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_tile_n: int = 0,
-             gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0, variant: int = VARIANT_AUTO,
-             stream=None):
+             gemm_group_m: int = 0, gemm_k_chunk: int = 0, gemm_cluster: int = 0, gemm_split_k: int = 0,
+             variant: int = VARIANT_AUTO, stream=None):
     """The widened contraction (include/poot_linear.h, poot_contract).
 
     x [M,K], w [N,K] and b [N] (or None) are float16 or bfloat16 CUDA
@@ -294,7 +297,7 @@ def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_ti
         out = torch.empty(yshape, dtype=ydt, device=x.device)
     elif out.dtype != ydt or tuple(out.shape) != yshape or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous {yshape} {ydt} tensor")
-    opts = options(variant, 0, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster)
+    opts = options(variant, 0, gemm_tile_n, gemm_group_m, gemm_k_chunk, gemm_cluster, gemm_split_k)
     bp = b.data_ptr() if b is not None else 0
     with torch.cuda.device(x.device):
         s = torch.cuda.current_stream(x.device) if stream is None else stream

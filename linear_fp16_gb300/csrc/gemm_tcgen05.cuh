@@ -75,6 +75,10 @@ struct GemmArgs {
   // step operands [groups*M, ld]
   int groups;
   int tiles_per_group;
+  // split K (GEN only, groups == split_k > 1): "group" g is split g of one
+  // contraction, summing K blocks g*num_k_blocks .. (g+1)*num_k_blocks-1 of x
+  // and W (no row offsets) into the FP32 partial tile y32 + g*M*N
+  int split_k;
 };
 
 // Activation step over the 16 packed pairs of one 32-column box (kept out of
@@ -356,7 +360,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           // rows of this group in the flattened x [groups*M, K] and W [groups*N, K]
           // (a tile that overhangs its group reads rows of the next one; they
           // only reach output rows or columns that are never stored)
-          const int xrow0 = g * args.M, wrow0 = g * args.N;
+          const bool ksplit = GEN && args.split_k > 1;
+          const int xrow0 = ksplit ? 0 : g * args.M, wrow0 = ksplit ? 0 : g * args.N;
+          const int kofs = ksplit ? g * num_kb * kGemmBK : 0;  // this split's first K element
           for (int kb = 0; kb < num_kb; kb += step) {
             const uint32_t eb = paired ? bar_empty(stage >> 1) : bar_empty(stage);
             if (paired && ck == STAGES - 2 && ch > 0) {
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               if (!mbar_wait(bar_cempty(ch & 1), (uint32_t)(((ch >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
             }
             for (int h = 0; h < step; ++h) {
-              const int st = stage + h, kc = (kb + h) * kGemmBK;
+              const int st = stage + h, kc = kofs + (kb + h) * kGemmBK;
               const uint32_t fb = bar_full(st);
               if constexpr (PAIR) {
                 // both CTAs' bytes complete on the even CTA's barrier
@@ -428,17 +434,19 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       for (int t = unit; t < args.num_tiles && ok; t += units) {
         int g, mb, nb;
         tile_decode(t, g, mb, nb);
-        const __half* xg = args.x + (size_t)g * args.M * args.K;
-        const __half* wg = args.w + (size_t)g * args.N * args.K;
+        const bool ksplit = GEN && args.split_k > 1;
+        const __half* xg = ksplit ? args.x : args.x + (size_t)g * args.M * args.K;
+        const __half* wg = ksplit ? args.w : args.w + (size_t)g * args.N * args.K;
+        const int kofs = ksplit ? g * num_kb * kGemmBK : 0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (MODE == kLoadCpAsync4) {
             if (w8) {
-              gemm_copy_rows_cp<8>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
-              gemm_copy_rows_cp<8>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<8>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kofs + kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<8>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kofs + kb * kGemmBK, cw, lane);
             } else {
-              gemm_copy_rows_cp<4>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, cw, lane);
-              gemm_copy_rows_cp<4>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<4>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kofs + kb * kGemmBK, cw, lane);
+              gemm_copy_rows_cp<4>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kofs + kb * kGemmBK, cw, lane);
             }
             cp_async_commit();
             if (filled == LAG) {
@@ -450,8 +458,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               ++filled;
             }
           } else {
-            gemm_copy_tile<MODE>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kb * kGemmBK, pt);
-            gemm_copy_tile<MODE>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kb * kGemmBK, pt);
+            gemm_copy_tile<MODE>(stage_a(stage), xg, kGemmBM, mb * kGemmBM, args.M, args.K, kofs + kb * kGemmBK, pt);
+            gemm_copy_tile<MODE>(stage_b(stage), wg, BN, nb * BN, args.N, args.K, kofs + kb * kGemmBK, pt);
             fence_proxy_async_smem();
             mbar_arrive(bar_full(stage));
           }

@@ -6,12 +6,15 @@
 
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "poot_linear.h"
 #include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
+#include "splitk.cuh"
 
 namespace {
 
@@ -36,6 +39,7 @@ thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 struct DeviceState {
   bool ready = false;
   int status = POOT_OK;  // POOT_OK or POOT_ERR_UNSUPPORTED_DEVICE / CUDA
+  int dev = 0;
   int sm_count = 0;
   int max_clusters4 = 0;  // co-resident 4-CTA clusters of the GEMM kernel
 };
@@ -128,6 +132,7 @@ int device_state(int* dev_out, DeviceState** st_out) {
       int mc4 = 0;
       if ((e = query_max_clusters4(&mc4)) != cudaSuccess) return cuda_fail(e);
       st.max_clusters4 = mc4;
+      st.dev = dev;
       st.sm_count = sms;
       st.status = POOT_OK;
       st.ready = true;
@@ -259,6 +264,7 @@ struct GemmPlan {
   int bn, stages, group_m, chunk_kb;
   int cluster;  // 1: single CTAs; 2: CTA pairs (2-SM MMA); 4: two pairs sharing x
   bool pair;    // cluster >= 2 (256-row tiles)
+  int split;    // K ranges (split-K); 1 = none
 };
 
 // Tile plan from a cost model: each CTA runs ceil(tiles / SMs) tiles; a
@@ -269,7 +275,7 @@ struct GemmPlan {
 // epilogue work per FLOP) were measured on GB300 for 224 (0.90 - 0.97) and
 // extrapolated below it.  Ties go to the wider tile.
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, int bn_req, int group_req,
-                   int chunk_req, int cluster_req, bool tma) {
+                   int chunk_req, int cluster_req, int split_req, bool allow_split, bool tma) {
   // CTA pairs (2-SM MMA) from M = 256 (one full pair tile); single CTAs
   // when M is smaller, for short K in one wave, or when the operands need
   // copies.
@@ -311,7 +317,47 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, 
   }
   if (bn_req != 0) best_bn = bn_req;
   else if (cluster == 1 && short_k_wave) best_bn = 64;  // most CTAs loading at once
+  // Split-K, planned jointly with the tile width, when one wave of tiles
+  // leaves more than a quarter of the CTA slots idle and K is long (or when
+  // a split is requested without a tile width).  Here a tile's cost is
+  // fitted to interleaved GB300 timings of every (width, split) filling at
+  // most one wave on M = 64 .. 256, N x K = 1024 x 16384 .. 14336 x 4096 (the
+  // chosen plan within 4% of the best measured on each): narrow tiles lose
+  // less than above (their many CTAs stream W in parallel), and a split
+  // costs about 4 us (the second kernel, the workspace's write and read)
+  // plus its bytes.
+  int split = split_req > 1 ? split_req : 1;
+  {
+    const int64_t tiles1 = num_m * ((N + best_bn - 1) / best_bn);
+    const bool underfilled = tiles1 <= slots && tiles1 * 4 < slots * 3;
+    const bool plan_joint = allow_split && cluster <= 2 &&
+                            ((split_req == 0 && num_kb >= 16 && underfilled) || (split_req > 1 && bn_req == 0));
+    if (plan_joint) {
+      static const int eff_split[] = {100, 93, 88, 83, 86, 78, 70};
+      static const int splits[] = {1, 2, 4, 8, 16};
+      int64_t best_cost = INT64_MAX;
+      int jbn = best_bn, jsplit = split;
+      for (int i = 0; i < 7; ++i) {
+        const int bn = cands[i];
+        if (bn_req != 0 && bn != bn_req) continue;
+        const int64_t tiles = num_m * ((N + bn - 1) / bn);
+        for (int j = 0; j < 5; ++j) {
+          const int S = splits[j];
+          if (split_req > 1 && S != split_req) continue;
+          if (split_req == 0 && S > 1 && (num_kb % S != 0 || num_kb / S < 8 || tiles * S > slots)) continue;
+          const int64_t waves = (tiles * S + slots - 1) / slots;
+          const int64_t per_kb = (2 * bn > 128 + bn) ? 2 * bn : 128 + bn;
+          int64_t cost = waves * ((num_kb / S) * per_kb * 100 / eff_split[i] + 1000);
+          if (S > 1) cost += 8000 + int64_t(S) * M * N * 4 / 1024;
+          if (cost < best_cost) { best_cost = cost; jbn = bn; jsplit = S; }
+        }
+      }
+      best_bn = jbn;
+      split = jsplit;
+    }
+  }
   GemmPlan p;
+  p.split = split;
   p.cluster = cluster;
   p.pair = pair;
   p.bn = best_bn;
@@ -334,6 +380,100 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, 
   return p;
 }
 
+// ---- split-K workspace ------------------------------------------------------
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::vector<void*> g_ws_retired;
+
+struct WorkspaceRelease {
+  ~WorkspaceRelease() {
+    for (auto& kv : g_ws)
+      if (kv.second.ptr != nullptr) cudaFree(kv.second.ptr);
+    for (void* p : g_ws_retired) cudaFree(p);
+  }
+} g_ws_release;
+
+// FP32 workspace of a split-K launch.  Outside stream capture: one buffer per
+// (device, stream), grown by doubling and kept for the life of the process
+// (calls on one stream are ordered, so they can share it; a buffer outgrown
+// is kept too, as work queued earlier may still read it).  Under capture:
+// a graph-owned allocation (cudaMallocAsync / cudaFreeAsync on the capturing
+// stream become memory nodes of the graph), so that a graph never shares a
+// buffer with calls made outside it.  nullptr: no workspace, no split.
+struct WorkspaceLease {
+  void* ptr = nullptr;
+  bool graph_owned = false;
+  cudaStream_t stream = nullptr;
+  // a graph-owned workspace is freed on its stream after the last kernel
+  // that reads it (or on any early return before those launches)
+  cudaError_t release() {
+    cudaError_t e = cudaSuccess;
+    if (graph_owned) e = cudaFreeAsync(ptr, stream);
+    graph_owned = false;
+    return e;
+  }
+  WorkspaceLease() = default;
+  WorkspaceLease(const WorkspaceLease&) = delete;
+  WorkspaceLease& operator=(const WorkspaceLease&) = delete;
+  WorkspaceLease(WorkspaceLease&& o) noexcept : ptr(o.ptr), graph_owned(o.graph_owned), stream(o.stream) {
+    o.graph_owned = false;
+  }
+  WorkspaceLease& operator=(WorkspaceLease&& o) noexcept {
+    if (this != &o) {
+      (void)release();
+      ptr = o.ptr;
+      graph_owned = o.graph_owned;
+      stream = o.stream;
+      o.graph_owned = false;
+    }
+    return *this;
+  }
+  ~WorkspaceLease() { (void)release(); }
+};
+
+WorkspaceLease stream_workspace(int dev, cudaStream_t stream, size_t bytes) {
+  WorkspaceLease lease;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return lease;
+  }
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (cs != cudaStreamCaptureStatusActive || cudaMallocAsync(&lease.ptr, bytes, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      lease.ptr = nullptr;
+      return lease;
+    }
+    lease.graph_owned = true;
+    lease.stream = stream;
+    return lease;
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace& ws = g_ws[std::make_pair(dev, stream)];
+  if (ws.bytes >= bytes) {
+    lease.ptr = ws.ptr;
+    return lease;
+  }
+  size_t want = bytes > 2 * ws.bytes ? bytes : 2 * ws.bytes;
+  want = (want + (size_t(1) << 20) - 1) & ~((size_t(1) << 20) - 1);
+  void* p = nullptr;
+  if (cudaMalloc(&p, want) != cudaSuccess) {
+    (void)cudaGetLastError();  // no split-K then; not an error of the call
+    return lease;
+  }
+  if (ws.ptr != nullptr) g_ws_retired.push_back(ws.ptr);
+  ws.ptr = p;
+  ws.bytes = want;
+  lease.ptr = p;
+  return lease;
+}
+
+constexpr int kMaxSplitK = 16;
+
 // The widened contraction's epilogue, as checked by poot_contract.
 struct EpiConfig {
   int dtype, out_f32, num_steps;
@@ -344,9 +484,9 @@ struct EpiConfig {
 
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
                 int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
-                cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1) {
+                int split_req, cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1) {
   const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
-                                  cluster_req, variant == POOT_VARIANT_GEMM_TMA);
+                                  cluster_req, split_req, G == 1, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
   GemmArgs a;
   a.x = static_cast<const __half*>(x);
@@ -366,13 +506,28 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   if (a.group_m > a.num_m_blocks) a.group_m = a.num_m_blocks;
   a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
   if (plan.cluster == 4) a.num_n_blocks = (a.num_n_blocks + 1) / 2;  // tile pairs along N
-  a.num_k_blocks = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
+  const int64_t num_kb_all = (K + kGemmBK - 1) / kGemmBK;
   const int64_t tiles_per_group = int64_t(a.num_m_blocks) * a.num_n_blocks;
-  const int64_t tiles = tiles_per_group * G;
+  // a requested split must divide the K blocks (and is not for groups or
+  // clusters of four); the partial sums need a workspace
+  if (split_req > 1 && (G != 1 || plan.cluster > 2 || num_kb_all % split_req != 0)) return POOT_ERR_INVALID_ARG;
+  int S = plan.split;
+  WorkspaceLease lease;
+  if (S > 1) {
+    lease = stream_workspace(st.dev, stream, size_t(S) * M * N * sizeof(float));
+    if (lease.ptr == nullptr) {
+      if (split_req > 1) return cuda_fail(cudaErrorMemoryAllocation);
+      S = 1;
+    }
+  }
+  float* const ws = static_cast<float*>(lease.ptr);
+  a.num_k_blocks = static_cast<int>(num_kb_all / S);
+  const int64_t tiles = tiles_per_group * (S > 1 ? S : G);
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
   a.num_tiles = static_cast<int>(tiles);
-  a.groups = static_cast<int>(G);
+  a.groups = static_cast<int>(S > 1 ? S : G);
   a.tiles_per_group = static_cast<int>(tiles_per_group);
+  a.split_k = S;
   a.tma_store = (N % 8 == 0 && aligned(y, 16)) ? 1 : 0;
   a.general = epi != nullptr ? 1 : 0;
   a.dtype = epi != nullptr ? epi->dtype : POOT_DTYPE_F16;
@@ -388,6 +543,35 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     a.ep_ptr[s] = used ? static_cast<const uint16_t*>(epi->ptr[s]) : nullptr;
     a.ep_ld[s] = used ? epi->ld[s] : 0;
     a.ep_vec[s] = (used && a.ep_ptr[s] != nullptr && aligned(a.ep_ptr[s], 16) && a.ep_ld[s] % 8 == 0) ? 1 : 0;
+  }
+  // the reduce kernel applies the real epilogue after a split-K GEMM
+  SplitReduceArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  if (S > 1) {
+    ra.ws = ws;
+    ra.S = S;
+    ra.M = a.M;
+    ra.N = a.N;
+    ra.dtype = a.dtype;
+    ra.out_f32 = a.out_f32;
+    ra.has_bias = a.has_bias;
+    ra.num_steps = a.num_steps;
+    for (int s = 0; s < kEpiMaxSteps; ++s) {
+      ra.ep_op[s] = a.ep_op[s];
+      ra.ep_ptr[s] = a.ep_ptr[s];
+      ra.ep_ld[s] = a.ep_ld[s];
+    }
+    ra.b = reinterpret_cast<const uint16_t*>(b);
+    ra.y = a.out_f32 ? nullptr : static_cast<uint16_t*>(y);
+    ra.y32 = a.out_f32 ? static_cast<float*>(y) : nullptr;
+    // the GEMM writes the unrounded partial sums of each split
+    a.general = 1;
+    a.out_f32 = 1;
+    a.has_bias = 0;
+    a.num_steps = 0;
+    a.y32 = ws;
+    a.y_vec = (N % 4 == 0) ? 1 : 0;
+    a.tma_store = 0;
   }
   const bool bf16 = a.dtype == POOT_DTYPE_BF16;
   // Paired stages (see GemmArgs::paired) need an even ring and every chunk
@@ -426,32 +610,44 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   }
 
   cudaError_t e;
-  if (epi != nullptr) {
-    // the widened epilogue is compiled into its own instantiations (CTA
-    // pairs or single CTAs; clusters of four are not offered here)
+  if (epi != nullptr || S > 1) {
+    // the widened epilogue (and the split-K partial sums) are compiled into
+    // their own instantiations (CTA pairs or single CTAs; clusters of four
+    // are not offered here)
     if (plan.cluster == 4) return POOT_ERR_INVALID_ARG;
     if (plan.cluster == 2) {
       const int64_t pairs = st.sm_count / 2;
       const int grid = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
       e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 2, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
                            Layout::DYN_BYTES, stream, 2u, tx, tw, ty, a);
-      return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+    } else {
+      const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
+      switch (variant) {
+        case POOT_VARIANT_GEMM_TMA:
+          e = launch(gemm_f16_tcgen05_kernel<kLoadTma, 1, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                     Layout::DYN_BYTES, stream, tx, tw, ty, a);
+          break;
+        case POOT_VARIANT_GEMM_CPASYNC:
+          e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1, true>, dim3(grid),
+                     dim3(gemm_threads(kLoadCpAsync4)), Layout::DYN_BYTES, stream, tx, tw, ty, a);
+          break;
+        default:
+          e = launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1, true>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
+                     Layout::DYN_BYTES, stream, tx, tw, ty, a);
+          break;
+      }
     }
-    const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
-    switch (variant) {
-      case POOT_VARIANT_GEMM_TMA:
-        e = launch(gemm_f16_tcgen05_kernel<kLoadTma, 1, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
-                   Layout::DYN_BYTES, stream, tx, tw, ty, a);
-        break;
-      case POOT_VARIANT_GEMM_CPASYNC:
-        e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1, true>, dim3(grid),
-                   dim3(gemm_threads(kLoadCpAsync4)), Layout::DYN_BYTES, stream, tx, tw, ty, a);
-        break;
-      default:
-        e = launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1, true>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
-                   Layout::DYN_BYTES, stream, tx, tw, ty, a);
-        break;
+    if (e == cudaSuccess && S > 1) {
+      const bool vec = N % 4 == 0 && (ra.out_f32 ? aligned(y, 16) : aligned(y, 8));
+      const int64_t units = vec ? M * N / 4 : M * N;
+      int64_t blocks = (units + 255) / 256;
+      const int64_t cap = int64_t(st.sm_count) * 8;
+      if (blocks > cap) blocks = cap;
+      e = vec ? launch(splitk_reduce_kernel<4>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, ra)
+              : launch(splitk_reduce_kernel<1>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, ra);
     }
+    const cudaError_t f = lease.release();
+    if (e == cudaSuccess) e = f;
     return e == cudaSuccess ? POOT_OK : cuda_fail(e);
   }
   if (plan.cluster == 4) {
@@ -562,6 +758,8 @@ bool gemm_options_ok(const poot_linear_options& o) {
     return false;
   if (o.gemm_group_m < 0) return false;
   if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return false;
+  if (o.gemm_split_k < 0 || o.gemm_split_k > kMaxSplitK) return false;
+  if (o.gemm_split_k > 1 && o.gemm_cluster == 4) return false;
   return o.gemm_cluster == 0 || o.gemm_cluster == 1 || o.gemm_cluster == 2 || o.gemm_cluster == 4;
 }
 
@@ -605,7 +803,7 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
       return launch_gemv(variant, *st, x, w, b, y, M, N, K, gemv_wpr, stream);
     default:
       return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
-                         o.gemm_cluster, stream);
+                         o.gemm_cluster, o.gemm_split_k, stream);
   }
 }
 
@@ -666,12 +864,13 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
     return POOT_ERR_INVALID_ARG;
   }
   if (o.gemm_cluster == 2 && variant != POOT_VARIANT_GEMM_TMA) return POOT_ERR_INVALID_ARG;
+  if (o.gemm_split_k > 1 && G > 1) return POOT_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState* st = nullptr;
   const int rc = device_state(&dev, &st);
   if (rc != POOT_OK) return rc;
   return launch_gemm(variant, *st, x, w, b, y, M, N, K, o.gemm_tile_n, o.gemm_group_m, o.gemm_k_chunk,
-                     o.gemm_cluster, stream, &epi, G);
+                     o.gemm_cluster, o.gemm_split_k, stream, &epi, G);
 }
 
 }  // namespace

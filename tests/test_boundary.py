@@ -145,6 +145,21 @@ def test_bad_gemm_cluster(cluster):
         L.POOT_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("split", [-1, 17])
+def test_bad_gemm_split_k(split):
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 2048, L.options(gemm_split_k=split), 0) == \
+        L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(X, W, B, Y, 400, 64, 2048, _spec(), L.options(gemm_split_k=split), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
+def test_split_k_refused_with_clusters_of_four_and_groups():
+    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 2048, L.options(gemm_cluster=4, gemm_split_k=2), 0) == \
+        L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract_grouped(X, W, B, Y, 2, 400, 64, 2048, _spec(), L.options(gemm_split_k=2), 0) == \
+        L.POOT_ERR_INVALID_ARG
+
+
 def test_cluster_needs_the_tma_variant():
     assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64,
                                 L.options(L.VARIANT_GEMM_CPASYNC, gemm_cluster=2), 0) == L.POOT_ERR_INVALID_ARG
