@@ -274,6 +274,41 @@ POOT_API int poot_contract_grouped(const void* x, const void* w, const void* b, 
                                    int64_t N, int64_t K, const poot_contraction_spec* spec,
                                    const poot_linear_options* opts, poot_stream_t stream);
 
+/*
+ * Split-K without any allocation.  The pages have no counterpart to this
+ * entry point: it is a library addition for callers that must not allocate
+ * device memory — code that runs under a caching allocator holding the
+ * device's memory budget (a library cudaMalloc there can fail or fragment
+ * the pool), and serving loops with a fixed memory footprint that cannot
+ * take an allocation's implicit device synchronisation.
+ *
+ * Computes y = FP16(x . W^T) + b on the GEMM (never the GEMV, whatever M)
+ * exactly as poot_linear_f16_ex with gemm_split_k = split_k and the GEMM
+ * variant for these pointers (GEMM_TMA when x and w are 16-byte aligned and
+ * K % 8 == 0, else GEMM_CPASYNC when both are 4-byte aligned and K is even,
+ * else GEMM_REG): same tile plan, same summation order, hence the same
+ * bits.  The FP32 partial sums live in one device array compiled into the
+ * library, POOT_NOALLOC_SCRATCH_BYTES per device, instead of the per-stream
+ * workspace.
+ * split_k: 2 .. 16 and must divide ceil(K / 64); split_k * M * N * 4 must
+ *   not exceed POOT_NOALLOC_SCRATCH_BYTES.  Otherwise POOT_ERR_INVALID_ARG,
+ *   before any CUDA call, with nothing queued.  K >= 1.
+ * Other arguments, alignment, ownership and errors as poot_linear_f16.
+ * The array needs no clearing: every element a call reads was written
+ *   earlier in the same call.
+ * Sharing: the array is one per device, used by every call of this entry
+ *   point on that device (no other entry point touches it).  Calls whose
+ *   work can overlap in time — on different streams with no event or
+ *   synchronisation ordering them — race on it and give wrong results;
+ *   calls on one stream, or otherwise ordered, are safe.
+ * Setup: the first call on each device looks the array's address up
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *   that first call outside stream capture.
+ */
+#define POOT_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+POOT_API int poot_linear_f16_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M,
+                                            int64_t N, int64_t K, int split_k, poot_stream_t stream);
+
 /* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
 POOT_API int poot_linear_version(void);
 

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     poot_linear_status_string, poot_linear_version, variant_for,
     ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,
     EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract, poot_contract_grouped,
+    NOALLOC_SCRATCH_BYTES, poot_linear_f16_splitk_noalloc,
 )
 
 __version__ = "0.1.0"

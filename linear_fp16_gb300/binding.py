@@ -46,6 +46,7 @@ EP_SILU = 3
 EP_GELU_TANH = 4
 EP_GELU_ERF = 5
 EPILOGUE_MAX_STEPS = 4
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # POOT_NOALLOC_SCRATCH_BYTES
 EP_CODES = {"add": EP_ADD, "mul": EP_MUL, "silu": EP_SILU, "gelu_tanh": EP_GELU_TANH, "gelu_erf": EP_GELU_ERF}
 
 
@@ -92,6 +93,7 @@ EXPORTS = {
                                      ctypes.POINTER(Options), _VP]),
     "poot_contract_grouped": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64,
                                              ctypes.POINTER(ContractionSpec), ctypes.POINTER(Options), _VP]),
+    "poot_linear_f16_splitk_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP]),
 }
 
 _lock = threading.Lock()
@@ -140,6 +142,12 @@ def poot_linear_f16_ex(x: int, w: int, b: int, y: int, M: int, N: int, K: int, o
     """opts: an Options instance or None (everything automatic)."""
     ref = ctypes.byref(opts) if opts is not None else None
     return load_library().poot_linear_f16_ex(x, w, b, y, M, N, K, ref, stream)
+
+
+def poot_linear_f16_splitk_noalloc(x: int, w: int, b: int, y: int, M: int, N: int, K: int, split_k: int,
+                                   stream: int) -> int:
+    """Split-K with its partial sums in the library's fixed device array (no allocation)."""
+    return load_library().poot_linear_f16_splitk_noalloc(x, w, b, y, M, N, K, split_k, stream)
 
 
 def poot_linear_f16_variant(x: int, w: int, b: int, y: int, M: int, N: int, K: int) -> int:

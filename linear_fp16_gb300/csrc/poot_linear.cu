@@ -484,7 +484,8 @@ struct EpiConfig {
 
 int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w, const void* b, void* y,
                 int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
-                int split_req, cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1) {
+                int split_req, cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1,
+                float* fixed_ws = nullptr, size_t fixed_ws_bytes = 0) {
   const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
                                   cluster_req, split_req, G == 1, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
@@ -513,14 +514,17 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   if (split_req > 1 && (G != 1 || plan.cluster > 2 || num_kb_all % split_req != 0)) return POOT_ERR_INVALID_ARG;
   int S = plan.split;
   WorkspaceLease lease;
-  if (S > 1) {
+  if (S > 1 && fixed_ws != nullptr) {
+    // a caller-provided workspace (the no-allocation entry point)
+    if (size_t(S) * M * N * sizeof(float) > fixed_ws_bytes) return POOT_ERR_INVALID_ARG;
+  } else if (S > 1) {
     lease = stream_workspace(st.dev, stream, size_t(S) * M * N * sizeof(float));
     if (lease.ptr == nullptr) {
       if (split_req > 1) return cuda_fail(cudaErrorMemoryAllocation);
       S = 1;
     }
   }
-  float* const ws = static_cast<float*>(lease.ptr);
+  float* const ws = fixed_ws != nullptr ? fixed_ws : static_cast<float*>(lease.ptr);
   a.num_k_blocks = static_cast<int>(num_kb_all / S);
   const int64_t tiles = tiles_per_group * (S > 1 ? S : G);
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
@@ -873,6 +877,57 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
                      o.gemm_cluster, o.gemm_split_k, stream, &epi, G);
 }
 
+// ---- split-K without allocation -----------------------------------------------
+// The partial sums of poot_linear_f16_splitk_noalloc live in this array,
+// compiled into the library (one per device, in the module's global memory),
+// so that callers that must not allocate — under a caching allocator that
+// holds the device's memory budget, or in a serving loop that cannot take an
+// allocation's implicit synchronisation — still get split-K.  Every element
+// a call reads is written earlier in the same call, so it is never cleared.
+// Calls that overlap in time race on it (one array per device).
+static_assert(POOT_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+static __device__ __align__(256) float g_noalloc_scratch[POOT_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Address of the array on device `dev` (the current device), looked up once.
+int noalloc_scratch(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_addr[dev] = p;
+  }
+  *out = static_cast<float*>(g_noalloc_addr[dev]);
+  return POOT_OK;
+}
+
+int run_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
+                       int split_k, cudaStream_t stream) {
+  int rc = validate(x, w, b, y, M, N, K);
+  if (rc != POOT_OK) return rc;
+  if (split_k < 2 || split_k > kMaxSplitK) return POOT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return POOT_OK;
+  const int64_t num_kb = (K + kGemmBK - 1) / kGemmBK;
+  if (K == 0 || num_kb % split_k != 0) return POOT_ERR_INVALID_ARG;
+  // split_k * M * N * 4 <= the array, without overflow (M, N < 2^31)
+  if (M * N > int64_t(POOT_NOALLOC_SCRATCH_BYTES / sizeof(float)) / split_k) return POOT_ERR_INVALID_ARG;
+  int variant = POOT_VARIANT_GEMM_REG;
+  if (xw_tma_ok(x, w, K)) variant = POOT_VARIANT_GEMM_TMA;
+  else if (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) variant = POOT_VARIANT_GEMM_CPASYNC;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  rc = device_state(&dev, &st);
+  if (rc != POOT_OK) return rc;
+  float* scratch = nullptr;
+  rc = noalloc_scratch(dev, &scratch);
+  if (rc != POOT_OK) return rc;
+  return launch_gemm(variant, *st, x, w, b, y, M, N, K, 0, 0, 0, 0, split_k, stream, nullptr, 1, scratch,
+                     POOT_NOALLOC_SCRATCH_BYTES);
+}
+
 }  // namespace
 
 extern "C" {
@@ -886,6 +941,11 @@ int poot_contract_grouped(const void* x, const void* w, const void* b, void* y, 
                           int64_t K, const poot_contraction_spec* spec, const poot_linear_options* opts,
                           poot_stream_t stream) {
   return contract(x, w, b, y, G, M, N, K, spec, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_f16_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N,
+                                   int64_t K, int split_k, poot_stream_t stream) {
+  return run_splitk_noalloc(x, w, b, y, M, N, K, split_k, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
