@@ -382,9 +382,11 @@ def run_ours(args, rank, world, local):
         clocks = sampler.summary(wall0, wall1)
     total_ms = t_start.elapsed_time(t_end)
     step_ms = max_over_ranks(dist, total_ms / args.steps, dev)
-    # one kernel per step: its mean duration is the step time on the
+    # one kernel per step (two for GEMM_PACKED: the row copy, then the
+    # GEMM): the mean duration of the step's kernels is the step time on the
     # launching stream (graph replay keeps launches back to back)
     kern_ms = step_ms
+    launches_per_step = 2 if chosen == L.VARIANT_GEMM_PACKED else 1
     if L.poot_linear_device_status(sh) != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
     y = sets[(args.warmup + args.steps - 1) % copies][3]
@@ -461,11 +463,12 @@ def run_ours(args, rank, world, local):
 
     # ---- roofline of the dominant kernel -----------------------------------
     peaks, src = load_peaks()
-    gemm = chosen in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG)
+    gemm = chosen in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED)
     gemv_vec = "gemv_f16_rows_kernel" if M <= 2 else "gemv_f16_mma_kernel"
     kernel_name = {L.VARIANT_GEMM_TMA: "gemm_f16_tcgen05_kernel<tma>",
                    L.VARIANT_GEMM_CPASYNC: "gemm_f16_tcgen05_kernel<cpasync4>",
                    L.VARIANT_GEMM_REG: "gemm_f16_tcgen05_kernel<reg16>",
+                   L.VARIANT_GEMM_PACKED: "pack_rows_kernel + gemm_f16_tcgen05_kernel<tma>",
                    L.VARIANT_GEMV: gemv_vec, L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
                    }.get(chosen, "bias_only_kernel")
     kern_s = kern_ms * 1e-3
@@ -510,7 +513,7 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

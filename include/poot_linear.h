@@ -70,8 +70,17 @@ enum {
     POOT_VARIANT_GEMM_CPASYNC = 5,/* tcgen05 GEMM, 4-byte async copies for
                                      row pitches TMA cannot take
                                      (K even, x and W 4-byte aligned) */
-    POOT_VARIANT_GEMM_REG = 6     /* tcgen05 GEMM, 2-byte register copies
+    POOT_VARIANT_GEMM_REG = 6,    /* tcgen05 GEMM, 2-byte register copies
                                      (any K and alignment) */
+    POOT_VARIANT_GEMM_PACKED = 7  /* any K and alignment: a copy kernel
+                                     writes x and W with rows padded to a
+                                     16-byte pitch into the library's
+                                     workspace ((M + N) * ceil8(K) * 2
+                                     bytes, as for split-K), then the TMA
+                                     GEMM runs on the copies.  The choice
+                                     for M > 16 when TMA cannot read x or W
+                                     in place; if no workspace can be had it
+                                     runs as GEMM_CPASYNC or GEMM_REG */
 };
 
 /* Largest M served by the GEMV variants. */
@@ -97,7 +106,8 @@ enum {
  * Ownership: the caller owns all four buffers.  x, w and b are only read;
  *   every element of y is written.  y must not overlap x, w or b.  The
  *   library allocates nothing per call, except that a split-K plan (small
- *   M, long K; see gemm_split_k) takes its FP32 workspace from a buffer the
+ *   M, long K; see gemm_split_k) and the GEMM_PACKED variant (x or W not
+ *   readable by TMA in place) take their workspace from a buffer the
  *   library keeps per device and stream, allocating or growing it on first
  *   need (a graph-owned block under stream capture).
  * Errors: argument errors are found before any CUDA call and nothing is
@@ -247,8 +257,9 @@ typedef struct poot_contraction_spec {
  * Runs on the tcgen05 GEMM for every M (the GEMV kernels serve only
  * poot_linear_f16).  `opts` may be NULL; its GEMV fields and variants are
  * ignored except the GEMM ones.  Asynchronous; the caller owns every
- * buffer; the library allocates nothing except the split-K workspace
- * described under poot_linear_f16 (never for the grouped form).
+ * buffer; the library allocates nothing except the workspace described
+ * under poot_linear_f16 (split-K, never for the grouped form; the packed
+ * copies of x and W when TMA cannot read them in place).
  * Errors: POOT_ERR_INVALID_ARG for a NULL spec, x, w or y, K == 0, a bad
  * dtype, step code, step count, NULL operand or ld < N, steps with out_f32,
  * or y overlapping x, W, b or an operand; POOT_ERR_MISALIGNED for a pointer

@@ -30,10 +30,11 @@ VARIANT_GEMV_SCALAR = 3
 VARIANT_GEMM_TMA = 4
 VARIANT_GEMM_CPASYNC = 5
 VARIANT_GEMM_REG = 6
+VARIANT_GEMM_PACKED = 7
 VARIANT_NAMES = {
     VARIANT_NONE: "none", VARIANT_BIAS_ONLY: "bias_only", VARIANT_GEMV: "gemv",
     VARIANT_GEMV_SCALAR: "gemv_scalar", VARIANT_GEMM_TMA: "gemm_tma",
-    VARIANT_GEMM_CPASYNC: "gemm_cpasync", VARIANT_GEMM_REG: "gemm_reg",
+    VARIANT_GEMM_CPASYNC: "gemm_cpasync", VARIANT_GEMM_REG: "gemm_reg", VARIANT_GEMM_PACKED: "gemm_packed",
 }
 GEMV_MAX_M = 16
 

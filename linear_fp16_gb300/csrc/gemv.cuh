@@ -31,6 +31,7 @@ struct GemvArgs {
   int M, N, K;
   int wpr;  // warps per W row: 1, 2, 4 or 8
   int kc;   // K chunk staged in shared memory (multiple of 256)
+  int prefetch;  // tensor-core GEMV: bulk-prefetch each warp's W slice into L2 first
 };
 
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
@@ -272,10 +273,14 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
 // that permutation these registers are exactly the A (W) and B (x^T)
 // fragments of two m16n8k16 MMAs, and no shuffles are needed.  D[n][m]
 // accumulates y^T; warps meet in shared memory in a fixed order.
-// WARPS (8 or 16) split K: with few 16-row tiles per SM (N/16 < 2 SMs) 16
-// warps keep twice the W bytes of a tile in flight (GB300, 8 x 4096 x 4096:
-// 8.5 us against 10.1 us with 8); with many tiles 8 warps are better
-// (8 x 14336 x 4096: 23.6 us against 27.5 us).
+// WARPS (8 or 16) split K: up to four 16-row tiles per SM 16 warps keep
+// twice the W bytes of a tile in flight; with more tiles 8 warps are better.
+// The L2 bulk prefetch of each warp's slice pays only with few tiles (at
+// most two for every three SMs), where it adds bytes in flight; with more
+// it competes with the loads themselves.  GB300, M = 8, K = 4096, 16 warps:
+// N = 1024 4.9 us with the prefetch against 5.8 without; N = 4096 7.8 us
+// without against 8.4 with; N = 8192 14.2 us (8 warps 16.4); N = 14336 with
+// 8 warps 20.6 us (16 warps 22.2).
 constexpr int kGemvMmaWarpsFew = 16;
 constexpr int kGemvMmaWarpsMany = 8;
 
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
   const bool okA = nA < N, okB = nB < N, okx0 = g < M, okx1 = (NT > 1) && (g + 8 < M);
   // start this warp's K slice of its 16 W rows towards L2 while the
   // previous grid drains (lane 4g prefetches rows nA and nB)
-  if (t == 0 && k_end > k_begin) {
+  if (a.prefetch && t == 0 && k_end > k_begin) {
     if (okA) prefetch_l2_bulk(wa + k_begin, (uint32_t)(k_end - k_begin) * 2u);
     if (okB) prefetch_l2_bulk(wb + k_begin, (uint32_t)(k_end - k_begin) * 2u);
   }

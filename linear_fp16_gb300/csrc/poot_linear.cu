@@ -14,6 +14,7 @@
 #include "poot_linear.h"
 #include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
+#include "pack.cuh"
 #include "splitk.cuh"
 
 namespace {
@@ -211,8 +212,7 @@ int choose_variant(const void* x, const void* w, int64_t M, int64_t N, int64_t K
   const bool tma = xw_tma_ok(x, w, K);
   if (M <= POOT_GEMV_MAX_M) return tma ? POOT_VARIANT_GEMV : POOT_VARIANT_GEMV_SCALAR;
   if (tma) return POOT_VARIANT_GEMM_TMA;
-  if (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) return POOT_VARIANT_GEMM_CPASYNC;
-  return POOT_VARIANT_GEMM_REG;
+  return POOT_VARIANT_GEMM_PACKED;
 }
 
 // Whether a forced variant's preconditions hold.
@@ -226,16 +226,18 @@ bool variant_applicable(int v, const void* x, const void* w, int64_t M, int64_t 
     case POOT_VARIANT_GEMM_TMA: return !empty && K > 0 && xw_tma_ok(x, w, K);
     case POOT_VARIANT_GEMM_CPASYNC: return !empty && K > 0 && K % 2 == 0 && aligned(x, 4) && aligned(w, 4);
     case POOT_VARIANT_GEMM_REG: return !empty && K > 0;
+    case POOT_VARIANT_GEMM_PACKED: return !empty && K > 0;
     default: return false;
   }
 }
 
 // Row-major [outer, inner] tensor of 2-byte elements (binary16, or bfloat16
-// when bf16), box [box_outer, box_inner].
+// when bf16), rows `pitch` elements apart (default inner), box [box_outer,
+// box_inner].
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-               uint32_t box_outer, CUtensorMapSwizzle swizzle, bool bf16 = false) {
+               uint32_t box_outer, CUtensorMapSwizzle swizzle, bool bf16 = false, uint64_t pitch = 0) {
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {(pitch != 0 ? pitch : inner) * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode_tiled(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -486,6 +488,11 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
                 int64_t M, int64_t N, int64_t K, int bn_req, int group_req, int chunk_req, int cluster_req,
                 int split_req, cudaStream_t stream, const EpiConfig* epi = nullptr, int64_t G = 1,
                 float* fixed_ws = nullptr, size_t fixed_ws_bytes = 0) {
+  // GEMM_PACKED: x and W are first copied into 16-byte-pitched rows in the
+  // workspace, then the TMA kernels run on the copies
+  const bool packed = variant == POOT_VARIANT_GEMM_PACKED;
+  if (packed && fixed_ws != nullptr) return POOT_ERR_INVALID_ARG;
+  if (packed) variant = POOT_VARIANT_GEMM_TMA;
   const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
                                   cluster_req, split_req, G == 1, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
@@ -514,17 +521,40 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   if (split_req > 1 && (G != 1 || plan.cluster > 2 || num_kb_all % split_req != 0)) return POOT_ERR_INVALID_ARG;
   int S = plan.split;
   WorkspaceLease lease;
+  // workspace: [packed x | packed W | split-K partial sums], 256-byte aligned parts
+  const int64_t Kp = (K + 7) / 8 * 8;
+  auto round256 = [](size_t v) { return (v + 255) & ~size_t(255); };
+  const size_t pack_x = packed ? round256(size_t(G) * M * Kp * 2) : 0;
+  const size_t pack_w = packed ? round256(size_t(G) * N * Kp * 2) : 0;
   if (S > 1 && fixed_ws != nullptr) {
     // a caller-provided workspace (the no-allocation entry point)
     if (size_t(S) * M * N * sizeof(float) > fixed_ws_bytes) return POOT_ERR_INVALID_ARG;
-  } else if (S > 1) {
-    lease = stream_workspace(st.dev, stream, size_t(S) * M * N * sizeof(float));
+  } else if (S > 1 || packed) {
+    const size_t split_bytes = S > 1 ? size_t(S) * M * N * sizeof(float) : 0;
+    lease = stream_workspace(st.dev, stream, pack_x + pack_w + split_bytes);
+    if (lease.ptr == nullptr && packed) {
+      // no room for the copies: the copy producers read x and W in place
+      // (they cannot feed CTA pairs)
+      if (cluster_req >= 2) return cuda_fail(cudaErrorMemoryAllocation);
+      const int fallback = (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) ? POOT_VARIANT_GEMM_CPASYNC
+                                                                          : POOT_VARIANT_GEMM_REG;
+      return launch_gemm(fallback, st, x, w, b, y, M, N, K, bn_req, group_req, chunk_req, cluster_req, split_req,
+                         stream, epi, G);
+    }
     if (lease.ptr == nullptr) {
       if (split_req > 1) return cuda_fail(cudaErrorMemoryAllocation);
       S = 1;
     }
   }
-  float* const ws = fixed_ws != nullptr ? fixed_ws : static_cast<float*>(lease.ptr);
+  char* const ws_base = static_cast<char*>(lease.ptr);
+  uint16_t* const xp = packed ? reinterpret_cast<uint16_t*>(ws_base) : nullptr;
+  uint16_t* const wp = packed ? reinterpret_cast<uint16_t*>(ws_base + pack_x) : nullptr;
+  float* const ws = fixed_ws != nullptr ? fixed_ws
+                    : (S > 1 ? reinterpret_cast<float*>(ws_base + pack_x + pack_w) : nullptr);
+  if (packed) {
+    a.x = reinterpret_cast<const __half*>(xp);
+    a.w = reinterpret_cast<const __half*>(wp);
+  }
   a.num_k_blocks = static_cast<int>(num_kb_all / S);
   const int64_t tiles = tiles_per_group * (S > 1 ? S : G);
   if (tiles > INT32_MAX) return POOT_ERR_INVALID_ARG;
@@ -599,10 +629,14 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   std::memset(&ty, 0, sizeof(ty));
   if (variant == POOT_VARIANT_GEMM_TMA) {
     // x and W of all groups as one flattened [G*M, K] and [G*N, K] tensor
-    if (!encode_2d(&tx, x, K, G * M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B, bf16) ||
-        !encode_2d(&tw, w, K, G * N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
-                   CU_TENSOR_MAP_SWIZZLE_128B, bf16))
+    // (the packed copies: rows Kp elements apart, inner extent still K)
+    const void* xs = packed ? static_cast<const void*>(xp) : x;
+    const void* wsrc = packed ? static_cast<const void*>(wp) : w;
+    const uint64_t pitch = packed ? static_cast<uint64_t>(Kp) : 0;
+    if (!encode_2d(&tx, xs, K, G * M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B, bf16, pitch) ||
+        !encode_2d(&tw, wsrc, K, G * N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
+                   CU_TENSOR_MAP_SWIZZLE_128B, bf16, pitch))
       return cuda_fail(cudaErrorInvalidValue);
   }
   if (a.tma_store) {
@@ -614,6 +648,23 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   }
 
   cudaError_t e;
+  if (packed) {
+    PackArgs pa;
+    pa.src[0] = static_cast<const uint16_t*>(x);
+    pa.src[1] = static_cast<const uint16_t*>(w);
+    pa.dst[0] = xp;
+    pa.dst[1] = wp;
+    pa.rows[0] = G * M;
+    pa.rows[1] = G * N;
+    pa.K = static_cast<int>(K);
+    pa.Kp = static_cast<int>(Kp);
+    const int64_t chunks = (G * M + G * N) * (Kp / 8);
+    int64_t blocks = (chunks + 255) / 256;
+    const int64_t cap = int64_t(st.sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    e = launch(pack_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pa);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if (epi != nullptr || S > 1) {
     // the widened epilogue (and the split-K partial sums) are compiled into
     // their own instantiations (CTA pairs or single CTAs; clusters of four
@@ -723,6 +774,7 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   a.K = static_cast<int>(K);
   a.wpr = wpr;
   a.kc = static_cast<int>(kc);
+  a.prefetch = 0;
   const int rows_per_block = kGemvWarps / wpr;
   const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
   if (blocks > INT32_MAX) return POOT_ERR_INVALID_ARG;
@@ -737,10 +789,12 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
       e = launch(gemv_f16_rows_kernel<2>, rgrid, dim3(kGemvRowThreads), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV && wpr_req == 0) {
     // 3 <= M <= 16 on the tensor cores, 16 rows of W per block; 16 warps
-    // along K when there are fewer than two such blocks per SM
+    // along K up to four such blocks per SM, the L2 prefetch up to two
+    // blocks for every three SMs
     const int64_t tiles = (N + 15) / 16;
     const dim3 mgrid(static_cast<unsigned>(tiles));
-    const bool few = tiles < 2 * int64_t(st.sm_count);
+    const bool few = tiles < 4 * int64_t(st.sm_count);
+    a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
     constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
     if (M <= 8)
       e = few ? launch(gemv_f16_mma_kernel<1, WF>, mgrid, dim3(WF * 32), 0, stream, a)
@@ -773,11 +827,12 @@ int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t
   if (rc != POOT_OK) return rc;
   int variant = o.variant;
   const int gemv_wpr = o.gemv_warps_per_row;
-  if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_REG) return POOT_ERR_INVALID_ARG;
+  if (variant < POOT_VARIANT_AUTO || variant > POOT_VARIANT_GEMM_PACKED) return POOT_ERR_INVALID_ARG;
   if (gemv_wpr != 0 && gemv_wpr != 1 && gemv_wpr != 2 && gemv_wpr != 4 && gemv_wpr != 8)
     return POOT_ERR_INVALID_ARG;
   if (!gemm_options_ok(o)) return POOT_ERR_INVALID_ARG;
-  if (o.gemm_cluster > 1 && variant != POOT_VARIANT_AUTO && variant != POOT_VARIANT_GEMM_TMA)
+  if (o.gemm_cluster > 1 && variant != POOT_VARIANT_AUTO && variant != POOT_VARIANT_GEMM_TMA &&
+      variant != POOT_VARIANT_GEMM_PACKED)
     return POOT_ERR_INVALID_ARG;
   if (variant == POOT_VARIANT_AUTO) {
     variant = choose_variant(x, w, M, N, K);
@@ -844,7 +899,7 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
   if (opts != nullptr) o = *opts;
   if (!gemm_options_ok(o) || o.gemm_cluster == 4) return POOT_ERR_INVALID_ARG;
   if (o.variant != POOT_VARIANT_AUTO && o.variant != POOT_VARIANT_GEMM_TMA && o.variant != POOT_VARIANT_GEMM_CPASYNC &&
-      o.variant != POOT_VARIANT_GEMM_REG)
+      o.variant != POOT_VARIANT_GEMM_REG && o.variant != POOT_VARIANT_GEMM_PACKED)
     return POOT_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return POOT_OK;
   if (K == 0 || x == nullptr || w == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
@@ -861,13 +916,12 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
   }
   int variant = o.variant;
   if (variant == POOT_VARIANT_AUTO) {
-    if (xw_tma_ok(x, w, K)) variant = POOT_VARIANT_GEMM_TMA;
-    else if (K % 2 == 0 && aligned(x, 4) && aligned(w, 4)) variant = POOT_VARIANT_GEMM_CPASYNC;
-    else variant = POOT_VARIANT_GEMM_REG;
+    variant = xw_tma_ok(x, w, K) ? POOT_VARIANT_GEMM_TMA : POOT_VARIANT_GEMM_PACKED;
   } else if (!variant_applicable(variant, x, w, M, N, K)) {
     return POOT_ERR_INVALID_ARG;
   }
-  if (o.gemm_cluster == 2 && variant != POOT_VARIANT_GEMM_TMA) return POOT_ERR_INVALID_ARG;
+  if (o.gemm_cluster == 2 && variant != POOT_VARIANT_GEMM_TMA && variant != POOT_VARIANT_GEMM_PACKED)
+    return POOT_ERR_INVALID_ARG;
   if (o.gemm_split_k > 1 && G > 1) return POOT_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState* st = nullptr;

@@ -54,8 +54,8 @@ def test_status_strings():
     (16, 4096, 4096, L.VARIANT_GEMV),
     (17, 4096, 4096, L.VARIANT_GEMM_TMA),
     (1024, 1024, 768, L.VARIANT_GEMM_TMA),
-    (2047, 1000, 770, L.VARIANT_GEMM_CPASYNC),
-    (100, 100, 771, L.VARIANT_GEMM_REG),
+    (2047, 1000, 770, L.VARIANT_GEMM_PACKED),
+    (100, 100, 771, L.VARIANT_GEMM_PACKED),
     (3, 10, 771, L.VARIANT_GEMV_SCALAR),
     (3, 10, 0, L.VARIANT_BIAS_ONLY),
     (0, 10, 5, L.VARIANT_NONE),
@@ -66,9 +66,10 @@ def test_variant_choice(M, N, K, want):
 
 
 def test_variant_choice_follows_alignment():
-    # 16-byte alignment of x and W selects TMA; 4-byte selects cp.async
-    assert L.poot_linear_f16_variant(X + 4, W, B, Y, 100, 64, 64) == L.VARIANT_GEMM_CPASYNC
-    assert L.poot_linear_f16_variant(X, W + 2, B, Y, 100, 64, 64) == L.VARIANT_GEMM_REG
+    # 16-byte alignment of x and W selects TMA in place; anything else the
+    # packed copies (the copy producers only when forced)
+    assert L.poot_linear_f16_variant(X + 4, W, B, Y, 100, 64, 64) == L.VARIANT_GEMM_PACKED
+    assert L.poot_linear_f16_variant(X, W + 2, B, Y, 100, 64, 64) == L.VARIANT_GEMM_PACKED
     assert L.poot_linear_f16_variant(X + 8, W, B, Y, 4, 64, 64) == L.VARIANT_GEMV_SCALAR
     # y alignment does not change the load variant (it only picks the store path)
     assert L.poot_linear_f16_variant(X, W, B, Y + 2, 100, 64, 64) == L.VARIANT_GEMM_TMA
@@ -114,7 +115,7 @@ def test_k_zero_needs_no_x_or_w():
     (L.VARIANT_GEMM_CPASYNC, 100, 65, 0), # odd K
     (L.VARIANT_BIAS_ONLY, 100, 64, 0),    # K != 0
     (L.VARIANT_NONE, 100, 64, 0),         # not empty
-    (7, 100, 64, 0),                      # unknown
+    (8, 100, 64, 0),                      # unknown
     (-2, 100, 64, 0),                     # unknown
 ])
 def test_inapplicable_forced_variant_is_rejected(variant, M, K, xoff):

@@ -18,7 +18,7 @@ from tests.parity import compare, legal_interval
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-GEMM_VARIANTS = [L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG]
+GEMM_VARIANTS = [L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED]
 GEMV_VARIANTS = [L.VARIANT_GEMV, L.VARIANT_GEMV_SCALAR]
 
 
@@ -171,7 +171,7 @@ def test_many_tiles_long_k():
 @pytest.mark.parametrize("variant", GEMM_VARIANTS)
 def test_every_tile_width(tile_n, variant):
     # ragged N against each tile width; K spans several K blocks and a tail
-    M, N, K = 300, 700, 200 if variant != L.VARIANT_GEMM_REG else 203
+    M, N, K = 300, 700, 200 if variant not in (L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED) else 203
     x, w, b = synth.make_inputs(M, N, K, "smallint", 60 + tile_n)
     if not _applicable(variant, M, K):
         pytest.skip("variant not applicable")
@@ -189,7 +189,7 @@ def test_tile_order_groups(group_m):
 def test_k_chunk_promotion(k_chunk, variant):
     # K = 1000 (1002 for odd-pitch copies): chunk boundaries inside and at
     # the end of the K range, a partial last chunk, and a single chunk
-    K = 1000 if variant != L.VARIANT_GEMM_REG else 1002
+    K = 1000 if variant not in (L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED) else 1002
     x, w, b = synth.make_inputs(260, 300, K, "smallint", 80 + k_chunk)
     _check(x, w, b, _gpu(x, w, b, variant, k_chunk=k_chunk), exact_ints=True)
     xn, wn, bn = synth.make_inputs(260, 300, K, "normal", 81 + k_chunk)
@@ -297,7 +297,7 @@ def test_unaligned_pointers_take_the_ragged_paths(M):
     wd.copy_(w)
     y = torch.empty((M, N), dtype=torch.float16, device=DEV)
     v = L.variant_for(xd, wd, b, y)
-    assert v in (L.VARIANT_GEMV_SCALAR, L.VARIANT_GEMM_REG)
+    assert v in (L.VARIANT_GEMV_SCALAR, L.VARIANT_GEMM_PACKED)
     L.linear(xd, wd, b.to(DEV), y)
     torch.cuda.synchronize()
     _check(x, w, b, _bits(y), exact_ints=True)
