@@ -25,11 +25,26 @@ enum EpiOp : int { kEpAdd = 1, kEpMul = 2, kEpSilu = 3, kEpGeluTanh = 4, kEpGelu
 constexpr int kEpiMaxSteps = 4;
 
 // round one FP32 value to the head dtype and back (exact widening)
+template <int DT>
+__device__ __forceinline__ float ep_rh_t(float v) {
+  if constexpr (DT == kEpiBf16) return __bfloat162float(__float2bfloat16_rn(v));
+  else return __half2float(__float2half_rn(v));
+}
 __device__ __forceinline__ float ep_rh(float v, int dt) {
   return dt == kEpiBf16 ? __bfloat162float(__float2bfloat16_rn(v)) : __half2float(__float2half_rn(v));
 }
 
 // two FP32 values rounded to the head dtype, packed low = first
+template <int DT>
+__device__ __forceinline__ uint32_t ep_pack_t(float a, float b) {
+  if constexpr (DT == kEpiBf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
 __device__ __forceinline__ uint32_t ep_pack(float a, float b, int dt) {
   if (dt == kEpiBf16) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -40,6 +55,11 @@ __device__ __forceinline__ uint32_t ep_pack(float a, float b, int dt) {
 }
 
 // a packed pair of head-dtype values, widened exactly to FP32
+template <int DT>
+__device__ __forceinline__ float2 ep_unpack_t(uint32_t u) {
+  if constexpr (DT == kEpiBf16) return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+  else return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
 __device__ __forceinline__ float2 ep_unpack(uint32_t u, int dt) {
   if (dt == kEpiBf16) return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
@@ -51,45 +71,68 @@ __device__ __forceinline__ float ep_widen(uint16_t bits, int dt) {
 }
 
 // x / (1 + exp(-x)) over Neg, Exp, Add, Div
-__device__ __forceinline__ float ep_silu(float t, int dt) {
-  const float e = ep_rh(expf(-t), dt);  // -t is exact
-  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
-  return ep_rh(__fdiv_rn(t, d), dt);
+template <int DT>
+__device__ __forceinline__ float ep_silu_t(float t) {
+  const float e = ep_rh_t<DT>(expf(-t));  // -t is exact
+  const float d = ep_rh_t<DT>(__fadd_rn(1.0f, e));
+  return ep_rh_t<DT>(__fdiv_rn(t, d));
 }
 
 // the tanh approximation in its sigmoid form: x / (1 + exp(-c2 (x + c1 x^3)))
 // c1 = RN(0.044715), c2 = RN(2 sqrt(2/pi)); the FP32 literals are within
 // 2^-24 relative of the exact constants, far from a rounding boundary of
 // either head dtype, so rounding them gives the same head values
-__device__ __forceinline__ float ep_gelu_tanh(float t, int dt) {
-  const float c1 = ep_rh(0.044715f, dt);
-  const float c2 = ep_rh(1.5957691216057308f, dt);
-  const float s = ep_rh(__fmul_rn(t, t), dt);
-  const float c = ep_rh(__fmul_rn(s, t), dt);
-  const float u = ep_rh(__fmul_rn(c1, c), dt);
-  const float v = ep_rh(__fadd_rn(t, u), dt);
-  const float z = ep_rh(__fmul_rn(c2, v), dt);
-  const float e = ep_rh(expf(-z), dt);
-  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
-  return ep_rh(__fdiv_rn(t, d), dt);
+template <int DT>
+__device__ __forceinline__ float ep_gelu_tanh_t(float t) {
+  const float c1 = ep_rh_t<DT>(0.044715f);
+  const float c2 = ep_rh_t<DT>(1.5957691216057308f);
+  const float s = ep_rh_t<DT>(__fmul_rn(t, t));
+  const float c = ep_rh_t<DT>(__fmul_rn(s, t));
+  const float u = ep_rh_t<DT>(__fmul_rn(c1, c));
+  const float v = ep_rh_t<DT>(__fadd_rn(t, u));
+  const float z = ep_rh_t<DT>(__fmul_rn(c2, v));
+  const float e = ep_rh_t<DT>(expf(-z));
+  const float d = ep_rh_t<DT>(__fadd_rn(1.0f, e));
+  return ep_rh_t<DT>(__fdiv_rn(t, d));
 }
 
 // 0.5 x (1 + erf(x / sqrt 2)) over Mul, Erf, Add; c3 = RN(1/sqrt 2)
-__device__ __forceinline__ float ep_gelu_erf(float t, int dt) {
-  const float c3 = ep_rh(0.70710678118654752f, dt);
-  const float s = ep_rh(__fmul_rn(c3, t), dt);
-  const float e = ep_rh(erff(s), dt);
-  const float d = ep_rh(__fadd_rn(1.0f, e), dt);
-  const float p = ep_rh(__fmul_rn(t, d), dt);
-  return ep_rh(__fmul_rn(0.5f, p), dt);
+template <int DT>
+__device__ __forceinline__ float ep_gelu_erf_t(float t) {
+  const float c3 = ep_rh_t<DT>(0.70710678118654752f);
+  const float s = ep_rh_t<DT>(__fmul_rn(c3, t));
+  const float e = ep_rh_t<DT>(erff(s));
+  const float d = ep_rh_t<DT>(__fadd_rn(1.0f, e));
+  const float p = ep_rh_t<DT>(__fmul_rn(t, d));
+  return ep_rh_t<DT>(__fmul_rn(0.5f, p));
+}
+
+template <int OP, int DT>
+__device__ __forceinline__ float ep_activation_t(float t) {
+  if constexpr (OP == kEpSilu) return ep_silu_t<DT>(t);
+  else if constexpr (OP == kEpGeluTanh) return ep_gelu_tanh_t<DT>(t);
+  else return ep_gelu_erf_t<DT>(t);
 }
 
 __device__ __forceinline__ float ep_activation(int op, float t, int dt) {
+  const bool bf = dt == kEpiBf16;
   switch (op) {
-    case kEpSilu: return ep_silu(t, dt);
-    case kEpGeluTanh: return ep_gelu_tanh(t, dt);
-    case kEpGeluErf: return ep_gelu_erf(t, dt);
+    case kEpSilu: return bf ? ep_silu_t<kEpiBf16>(t) : ep_silu_t<kEpiF16>(t);
+    case kEpGeluTanh: return bf ? ep_gelu_tanh_t<kEpiBf16>(t) : ep_gelu_tanh_t<kEpiF16>(t);
+    case kEpGeluErf: return bf ? ep_gelu_erf_t<kEpiBf16>(t) : ep_gelu_erf_t<kEpiF16>(t);
     default: return t;
+  }
+}
+
+// The activation OP over n packed pairs of head-dtype values, in place.
+// Unrolled so that several elements' dependent chains (exp, divide, the
+// roundings) are in flight at once.
+template <int OP, int DT, int N>
+__device__ __forceinline__ void ep_activation_pairs(uint32_t* v) {
+#pragma unroll 2
+  for (int i = 0; i < N; ++i) {
+    const float2 t = ep_unpack_t<DT>(v[i]);
+    v[i] = ep_pack_t<DT>(ep_activation_t<OP, DT>(t.x), ep_activation_t<OP, DT>(t.y));
   }
 }
 

@@ -82,11 +82,24 @@ struct GemmArgs {
 };
 
 // Activation step over the 16 packed pairs of one 32-column box (kept out of
-// line: the packed pairs pass through local memory only on this path).
+// line: the packed pairs pass through local memory only on this path).  The
+// op and dtype are dispatched once per box, so each loop body is
+// straight-line code.
 __device__ __noinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) {
-  for (int i = 0; i < 16; ++i) {
-    const float2 t = ep_unpack(v[i], dt);
-    v[i] = ep_pack(ep_activation(op, t.x, dt), ep_activation(op, t.y, dt), dt);
+  if (dt == kEpiBf16) {
+    switch (op) {
+      case kEpSilu: ep_activation_pairs<kEpSilu, kEpiBf16, 16>(v); break;
+      case kEpGeluTanh: ep_activation_pairs<kEpGeluTanh, kEpiBf16, 16>(v); break;
+      case kEpGeluErf: ep_activation_pairs<kEpGeluErf, kEpiBf16, 16>(v); break;
+      default: break;
+    }
+  } else {
+    switch (op) {
+      case kEpSilu: ep_activation_pairs<kEpSilu, kEpiF16, 16>(v); break;
+      case kEpGeluTanh: ep_activation_pairs<kEpGeluTanh, kEpiF16, 16>(v); break;
+      case kEpGeluErf: ep_activation_pairs<kEpGeluErf, kEpiF16, 16>(v); break;
+      default: break;
+    }
   }
 }
 
