@@ -661,9 +661,42 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           // bias of the box: lane l holds b[nc + l]; broadcast by shuffles
           const unsigned short blu = bias16[g];
           const int dt = GEN ? args.dtype : (int)kEpiF16;
+          if (GEN && args.out_f32 && args.tma_store) {
+            // FP32 output (the sum, + b rounded once in FP32) through the
+            // staging boxes: the 32-column box as two 32 x 16 FP32 boxes
+            // (64 bytes a row, the same 64-byte swizzle as the 16-bit box),
+            // each stored by TMA through an FP32 map that clips at M and N
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t packed[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float bj = ep_widen(__shfl_sync(0xffffffffu, blu, 16 * h + j), dt);
+                const float sj = acc[g * 32 + 16 * h + j];
+                packed[j] = __float_as_uint(args.has_bias ? __fadd_rn(sj, bj) : sj);
+              }
+              if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+              __syncwarp();
+              uint8_t* rowp = stg + sbuf * L::STG_BYTES + lane * 64;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int pos = j ^ ((lane >> 1) & 3);
+                *reinterpret_cast<uint4*>(rowp + pos * 16) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc + 16 * h, m0 + q * 32, grp);
+                bulk_commit_group();
+              }
+              sbuf ^= 1;
+            }
+            continue;
+          }
           if (GEN && args.out_f32) {
-            // FP32 output: the sum (+ b rounded once in FP32); lane = row,
-            // its 32 consecutive columns stored directly
+            // FP32 output without TMA (y32 not 16-byte aligned or N % 4 != 0):
+            // lane = row, its 32 consecutive columns stored directly
             const int row = m0 + q * 32 + lane;
             float* yr = args.y32 + ((size_t)grp * M + (row < M ? row : 0)) * N + nc;
 #pragma unroll

@@ -231,6 +231,19 @@ bool variant_applicable(int v, const void* x, const void* w, int64_t M, int64_t 
   }
 }
 
+// [slabs][outer][inner] tensor of FP32, box [1][box_outer][box_inner].
+bool encode_3d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t slabs,
+                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  const cuuint64_t dims[3] = {inner, outer, slabs};
+  const cuuint64_t strides[2] = {inner * 4, inner * outer * 4};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major [outer, inner] tensor of 2-byte elements (binary16, or bfloat16
 // when bf16), rows `pitch` elements apart (default inner), box [box_outer,
 // box_inner].
@@ -569,7 +582,8 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   a.has_bias = (epi == nullptr || b != nullptr) ? 1 : 0;
   a.y_vec = (N % 4 == 0 && aligned(y, 16)) ? 1 : 0;
   a.y32 = a.out_f32 ? static_cast<float*>(y) : nullptr;
-  if (a.out_f32) a.tma_store = 0;
+  // FP32 output: TMA stores of 32 x 16 boxes need 16-byte rows
+  if (a.out_f32) a.tma_store = (N % 4 == 0 && aligned(y, 16)) ? 1 : 0;
   a.num_steps = epi != nullptr ? epi->num_steps : 0;
   for (int s = 0; s < kEpiMaxSteps; ++s) {
     const bool used = s < a.num_steps;
@@ -605,7 +619,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     a.num_steps = 0;
     a.y32 = ws;
     a.y_vec = (N % 4 == 0) ? 1 : 0;
-    a.tma_store = 0;
+    a.tma_store = (N % 4 == 0) ? 1 : 0;  // the workspace is 256-byte aligned
   }
   const bool bf16 = a.dtype == POOT_DTYPE_BF16;
   // Paired stages (see GemmArgs::paired) need an even ring and every chunk
@@ -641,9 +655,15 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   }
   if (a.tma_store) {
     // the widened kernels store through [G][M][N] so that boxes clip at each
-    // group's M; the plain kernels through [M][N]
-    const bool ok = epi != nullptr ? encode_3d(&ty, y, N, M, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16)
-                                   : encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16);
+    // group's M (FP32 output, split-K partial sums included: [groups][M][N]
+    // FP32 with 32 x 16 boxes); the plain kernels through [M][N]
+    bool ok;
+    if (a.out_f32)
+      ok = encode_3d_f32(&ty, a.y32, N, M, a.groups, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    else if (epi != nullptr)
+      ok = encode_3d(&ty, y, N, M, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16);
+    else
+      ok = encode_2d(&ty, y, N, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, bf16);
     if (!ok) return cuda_fail(cudaErrorInvalidValue);
   }
 

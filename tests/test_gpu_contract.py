@@ -361,3 +361,19 @@ def test_grouped_leaves_other_groups_rows_alone():
     assert torch.all(buf[G * M] == 12345.0)
     want = oracle.contraction_grouped(_bits(x), _bits(w), _bits(b))
     assert np.array_equal(_bits(y), want)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_f32_output_store_paths(dt):
+    # N % 4 == 0 and a 16-byte aligned y: TMA stores of 32 x 16 FP32 boxes,
+    # clipped at a ragged M; the same y 4 bytes off its alignment: direct stores
+    M, N, K = 301, 264, 192
+    x, w, b = _inputs(M, N, K, "smallint", 330, dt)
+    y_tma = _gpu(x, w, b, out_f32=True)
+    _check_f32(x, w, b, y_tma, dt, exact_sums=True)
+    buf = torch.full((M * N + 1,), float("nan"), dtype=torch.float32, device=DEV)
+    y_off = buf[1:].view(M, N)
+    L.contract(x.to(DEV), w.to(DEV), b.to(DEV), out=y_off, out_f32=True)
+    torch.cuda.synchronize()
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    assert torch.equal(y_off.cpu(), y_tma)
