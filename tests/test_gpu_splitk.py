@@ -196,3 +196,42 @@ def test_stream_capture_uses_a_graph_owned_workspace():
         assert np.array_equal(_bits(y), eager)
     assert L.poot_linear_device_status(0) == L.POOT_OK
     _check(x, w, b, eager, exact_ints=True)
+
+
+# ---- long K and concurrent host threads -----------------------------------------
+@pytest.mark.parametrize("M,N", [(200, 300), (1, 520), (8, 264)])
+def test_k_65536_exact(M, N):
+    # |S| <= 65536 * 16 < 2^24: every FP32 partial sum is exact, so the result
+    # is bit-exact whatever the split and chunking (GEMM with automatic
+    # split for M = 200; the GEMVs for M = 1 and 8)
+    x, w, b = synth.make_inputs(M, N, 65536, "smallint", 996 + M)
+    _check(x, w, b, _lin(x, w, b), exact_ints=True)
+
+
+def test_two_host_threads_on_their_own_streams():
+    import threading
+    ins = [synth.make_inputs(128, 1024, 8192, "smallint", 997 + i) for i in range(2)]
+    dev = [tuple(t.to(DEV) for t in xwb) for xwb in ins]
+    ys = [torch.empty(128, 1024, dtype=torch.float16, device=DEV) for _ in range(2)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream(DEV)
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    L.linear(*dev[i], ys[i])   # automatic split-K: the stream's own workspace
+            s.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    th = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors, errors
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    for i in range(2):
+        _check(*ins[i], _bits(ys[i]), exact_ints=True)
