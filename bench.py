@@ -395,6 +395,22 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device-side wait timed out during the timed region")
     y = sets[(args.warmup + args.steps - 1) % copies][3]
 
+    # Per-launch distribution, after (and apart from) the timed region: each
+    # call launched eagerly between its own pair of events on the launching
+    # stream, rotating the input sets as the timed steps do (so it includes
+    # the host's launch latency that the graph-timed value leaves out).
+    reps = 200 if M <= L.GEMV_MAX_M else 50
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for r, (e0, e1) in enumerate(ev_pairs):
+        e0.record(stream)
+        step(args.warmup + args.steps + r, sh)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per_launch = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev_pairs)
+    per_launch_us = {"reps": reps, "median": per_launch[reps // 2], "p10": per_launch[reps // 10],
+                     "p90": per_launch[(9 * reps) // 10],
+                     "how": "eager launches, each between its own CUDA events (launch latency included)"}
+
     flops = 2.0 * M * N * K
     value = world * flops / (step_ms * 1e-3) / 1e12
 
@@ -518,6 +534,7 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
+        "per_launch_us": per_launch_us,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -10,7 +10,7 @@ from .binding import (  # noqa: F401
     POOT_ERR_MISALIGNED, POOT_ERR_UNSUPPORTED_DEVICE, POOT_OK, PootLinearError,
     VARIANT_AUTO, VARIANT_BIAS_ONLY, VARIANT_GEMM_CPASYNC, VARIANT_GEMM_REG,
     VARIANT_GEMM_TMA, VARIANT_GEMM_PACKED, VARIANT_GEMV, VARIANT_GEMV_SCALAR, VARIANT_NAMES, VARIANT_NONE,
-    library_path, linear, load_library, poot_linear_device_status, poot_linear_f16,
+    library_path, linear, load_library, poot_linear, poot_linear_device_status, poot_linear_f16,
     poot_linear_f16_ex, poot_linear_f16_variant, poot_linear_last_cuda_error,
     poot_linear_status_string, poot_linear_version, variant_for,
     ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,

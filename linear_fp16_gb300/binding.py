@@ -240,6 +240,9 @@ def linear(x, w, b, out=None, *, variant: int = VARIANT_AUTO, gemv_warps_per_row
     return out
 
 
+poot_linear = linear  # the tensor-level call under its C name's stem
+
+
 def variant_for(x, w, b, y) -> int:
     """The variant the library would choose for these tensors."""
     M, K = x.shape
