@@ -103,6 +103,8 @@ __device__ __noinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) 
   }
 }
 
+enum GemmEpi : int { kEpiPlain = 0, kEpiHead = 1, kEpiFull = 2 };
+
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;        // one 128-byte swizzle row of binary16
 constexpr int kGemmMaxBN = 256;
@@ -253,15 +255,20 @@ __device__ __forceinline__ void gemm_copy_rows_cp(uint32_t dst_base, const __hal
 // both, so a CTA reads 24 KB per stage from L2 instead of 32 KB.  A stage is
 // refilled only after both pairs' MMAs released it (each "empty" barrier
 // counts one multicast commit from each pair).
-// GEN: the widened contraction's epilogue (head dtype, optional bias, FP32
-// output, epilogue steps) is compiled in; without it the kernel has only the
-// plain binary16 epilogue and ignores the fields that select the rest.
-template <int MODE, int CL, bool GEN = false>
+// EPI selects the epilogue compiled in: kEpiPlain, the plain binary16
+// y = RN16(RN16(sum) + b) (the kernel ignores the fields that select the
+// rest); kEpiHead, the widened contraction's head dtype and optional bias
+// (groups included); kEpiFull, everything of the widened contraction (FP32
+// output, epilogue steps, split-K partial sums).  The lighter forms keep
+// fewer registers live in the epilogue.
+template <int MODE, int CL, int EPI = kEpiPlain>
 __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     gemm_f16_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_x,
                             const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_y, const GemmArgs args) {
   constexpr bool PAIR = CL >= 2;
+  constexpr bool GEN = EPI != kEpiPlain;  // the widened contraction's fields are read
+  constexpr bool FULL = EPI == kEpiFull;  // FP32 output, steps, split-K partial sums
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
   static_assert(!PAIR || MODE == kLoadTma, "the CTA-pair kernel loads through TMA only");
   using L = GemmLayout;
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           // rows of this group in the flattened x [groups*M, K] and W [groups*N, K]
           // (a tile that overhangs its group reads rows of the next one; they
           // only reach output rows or columns that are never stored)
-          const bool ksplit = GEN && args.split_k > 1;
+          const bool ksplit = FULL && args.split_k > 1;
           const int xrow0 = ksplit ? 0 : g * args.M, wrow0 = ksplit ? 0 : g * args.N;
           const int kofs = ksplit ? g * num_kb * kGemmBK : 0;  // this split's first K element
           for (int kb = 0; kb < num_kb; kb += step) {
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       for (int t = unit; t < args.num_tiles && ok; t += units) {
         int g, mb, nb;
         tile_decode(t, g, mb, nb);
-        const bool ksplit = GEN && args.split_k > 1;
+        const bool ksplit = FULL && args.split_k > 1;
         const __half* xg = ksplit ? args.x : args.x + (size_t)g * args.M * args.K;
         const __half* wg = ksplit ? args.w : args.w + (size_t)g * args.N * args.K;
         const int kofs = ksplit ? g * num_kb * kGemmBK : 0;
@@ -661,7 +668,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           // bias of the box: lane l holds b[nc + l]; broadcast by shuffles
           const unsigned short blu = bias16[g];
           const int dt = GEN ? args.dtype : (int)kEpiF16;
-          if (GEN && args.out_f32 && args.tma_store) {
+          if (FULL && args.out_f32 && args.tma_store) {
             // FP32 output (the sum, + b rounded once in FP32) through the
             // staging boxes: the 32-column box as two 32 x 16 FP32 boxes
             // (64 bytes a row, the same 64-byte swizzle as the 16-bit box),
@@ -694,7 +701,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             }
             continue;
           }
-          if (GEN && args.out_f32) {
+          if (FULL && args.out_f32) {
             // FP32 output without TMA (y32 not 16-byte aligned or N % 4 != 0):
             // lane = row, its 32 consecutive columns stored directly
             const int row = m0 + q * 32 + lane;
@@ -745,7 +752,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               packed[i] = t;
             }
             const int row = m0 + q * 32 + lane;
-            for (int s = 0; s < args.num_steps; ++s) {
+            for (int s = 0; s < (FULL ? args.num_steps : 0); ++s) {
               const int op = args.ep_op[s];
               if (op == kEpAdd || op == kEpMul) {
 #pragma unroll

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <type_traits>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -55,9 +56,9 @@ int cuda_fail(cudaError_t e) {
   return POOT_ERR_CUDA;
 }
 
-template <int MODE, int CL, bool GEN = false>
+template <int MODE, int CL, int EPI = kEpiPlain>
 cudaError_t set_gemm_attrs() {
-  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout::DYN_BYTES);
 }
 
@@ -117,10 +118,14 @@ int device_state(int* dev_out, DeviceState** st_out) {
           (e = set_gemm_attrs<kLoadTma, 4>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadCpAsync4, 1>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadReg16, 1>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadTma, 1, true>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadTma, 2, true>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadCpAsync4, 1, true>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadReg16, 1, true>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 1, kEpiHead>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 2, kEpiHead>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadCpAsync4, 1, kEpiHead>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadReg16, 1, kEpiHead>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 1, kEpiFull>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadTma, 2, kEpiFull>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadCpAsync4, 1, kEpiFull>()) != cudaSuccess ||
+          (e = set_gemm_attrs<kLoadReg16, 1, kEpiFull>()) != cudaSuccess ||
           (e = set_gemv_attrs<1, true>()) != cudaSuccess || (e = set_gemv_attrs<2, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<4, true>()) != cudaSuccess || (e = set_gemv_attrs<8, true>()) != cudaSuccess ||
           (e = set_gemv_attrs<16, true>()) != cudaSuccess ||
@@ -690,28 +695,32 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     // their own instantiations (CTA pairs or single CTAs; clusters of four
     // are not offered here)
     if (plan.cluster == 4) return POOT_ERR_INVALID_ARG;
-    if (plan.cluster == 2) {
-      const int64_t pairs = st.sm_count / 2;
-      const int grid = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
-      e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 2, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
-                           Layout::DYN_BYTES, stream, 2u, tx, tw, ty, a);
-    } else {
+    // head dtype and bias only: the lighter instantiation; FP32 output,
+    // steps or split-K partial sums: the full one
+    const bool full = S > 1 || a.out_f32 || a.num_steps > 0;
+    auto launch_widened = [&](auto epi_tag) -> cudaError_t {
+      constexpr int E = decltype(epi_tag)::value;
+      if (plan.cluster == 2) {
+        const int64_t pairs = st.sm_count / 2;
+        const int grid = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
+        return launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 2, E>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                                Layout::DYN_BYTES, stream, 2u, tx, tw, ty, a);
+      }
       const int grid = static_cast<int>(tiles < st.sm_count ? tiles : st.sm_count);
       switch (variant) {
         case POOT_VARIANT_GEMM_TMA:
-          e = launch(gemm_f16_tcgen05_kernel<kLoadTma, 1, true>, dim3(grid), dim3(gemm_threads(kLoadTma)),
-                     Layout::DYN_BYTES, stream, tx, tw, ty, a);
-          break;
+          return launch(gemm_f16_tcgen05_kernel<kLoadTma, 1, E>, dim3(grid), dim3(gemm_threads(kLoadTma)),
+                        Layout::DYN_BYTES, stream, tx, tw, ty, a);
         case POOT_VARIANT_GEMM_CPASYNC:
-          e = launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1, true>, dim3(grid),
-                     dim3(gemm_threads(kLoadCpAsync4)), Layout::DYN_BYTES, stream, tx, tw, ty, a);
-          break;
+          return launch(gemm_f16_tcgen05_kernel<kLoadCpAsync4, 1, E>, dim3(grid), dim3(gemm_threads(kLoadCpAsync4)),
+                        Layout::DYN_BYTES, stream, tx, tw, ty, a);
         default:
-          e = launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1, true>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
-                     Layout::DYN_BYTES, stream, tx, tw, ty, a);
-          break;
+          return launch(gemm_f16_tcgen05_kernel<kLoadReg16, 1, E>, dim3(grid), dim3(gemm_threads(kLoadReg16)),
+                        Layout::DYN_BYTES, stream, tx, tw, ty, a);
       }
-    }
+    };
+    e = full ? launch_widened(std::integral_constant<int, kEpiFull>{})
+             : launch_widened(std::integral_constant<int, kEpiHead>{});
     if (e == cudaSuccess && S > 1) {
       const bool vec = N % 4 == 0 && (ra.out_f32 ? aligned(y, 16) : aligned(y, 8));
       const int64_t units = vec ? M * N / 4 : M * N;
