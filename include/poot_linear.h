@@ -96,9 +96,11 @@ enum {
  *
  * x, w, b, y: device pointers (memory of the current device) to contiguous
  *   row-major binary16 data with the shapes above.  2-byte alignment is
- *   required; 16-byte alignment of x, w and y (and K % 8 == 0, N % 8 == 0)
- *   selects the TMA paths, anything else takes a slower path with the same
- *   results.
+ *   required.  With x and w 16-byte aligned and K % 8 == 0 the GEMM reads
+ *   them in place by TMA; otherwise (M > 16) it first copies them into
+ *   16-byte-pitched rows (GEMM_PACKED).  y 16-byte aligned with N % 8 == 0
+ *   is stored by TMA, else by plain stores.  Every path gives results
+ *   within the same contract.
  * M, N, K: sizes, 0 <= M, N, K < 2^31.  M == 0 or N == 0 launches nothing
  *   (pointers may then be NULL).  K == 0 gives y = b in every row (x and w
  *   may then be NULL).
@@ -154,10 +156,12 @@ typedef struct poot_linear_options {
                                 capture, a graph-owned allocation freed on
                                 the stream after the second kernel.  Not with
                                 gemm_cluster 4, nor with grouped contractions.
-                                Automatic splitting happens when the output
-                                tiles fill less than half of the SMs and K is
-                                at least 1024; when no workspace can be had,
-                                an automatic split falls back to none and a
+                                Automatic splitting happens when one wave of
+                                output tiles leaves more than a quarter of
+                                the SMs idle and K is at least 1024; the tile
+                                width and the split are then chosen
+                                together.  When no workspace can be had, an
+                                automatic split falls back to none and a
                                 requested one returns POOT_ERR_CUDA */
 } poot_linear_options;
 
