@@ -8,7 +8,9 @@
 #include <cstring>
 #include <map>
 #include <type_traits>
+#include <functional>
 #include <mutex>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -406,7 +408,19 @@ struct Workspace {
   size_t bytes = 0;
 };
 std::mutex g_ws_mu;
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// key: (device, stream, thread): the thread is part of the key only for
+// cudaStreamPerThread, one handle that names a different stream in each thread
+struct WorkspaceKey {
+  int dev;
+  cudaStream_t stream;
+  std::thread::id thread;
+  bool operator<(const WorkspaceKey& o) const {
+    if (dev != o.dev) return dev < o.dev;
+    if (stream != o.stream) return std::less<cudaStream_t>()(stream, o.stream);
+    return thread < o.thread;
+  }
+};
+std::map<WorkspaceKey, Workspace> g_ws;
 std::vector<void*> g_ws_retired;
 
 struct WorkspaceRelease {
@@ -417,8 +431,9 @@ struct WorkspaceRelease {
   }
 } g_ws_release;
 
-// FP32 workspace of a split-K launch.  Outside stream capture: one buffer per
-// (device, stream), grown by doubling and kept for the life of the process
+// Workspace of a call (split-K partial sums, packed operands).  Outside
+// stream capture: one buffer per (device, stream; thread for
+// cudaStreamPerThread), grown by doubling and kept for the life of the process
 // (calls on one stream are ordered, so they can share it; a buffer outgrown
 // is kept too, as work queued earlier may still read it).  Under capture:
 // a graph-owned allocation (cudaMallocAsync / cudaFreeAsync on the capturing
@@ -473,7 +488,8 @@ WorkspaceLease stream_workspace(int dev, cudaStream_t stream, size_t bytes) {
     return lease;
   }
   std::lock_guard<std::mutex> lock(g_ws_mu);
-  Workspace& ws = g_ws[std::make_pair(dev, stream)];
+  const std::thread::id tid = stream == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
+  Workspace& ws = g_ws[WorkspaceKey{dev, stream, tid}];
   if (ws.bytes >= bytes) {
     lease.ptr = ws.ptr;
     return lease;
