@@ -235,3 +235,35 @@ def test_two_host_threads_on_their_own_streams():
     assert L.poot_linear_device_status(0) == L.POOT_OK
     for i in range(2):
         _check(*ins[i], _bits(ys[i]), exact_ints=True)
+
+
+def test_per_thread_default_stream_handle_from_two_threads():
+    # cudaStreamPerThread (handle 2) names a different stream in each thread:
+    # each thread gets its own workspace
+    import threading
+    PER_THREAD = 2
+    ins = [synth.make_inputs(128, 1024, 8192, "smallint", 1990 + i) for i in range(2)]
+    dev = [tuple(t.to(DEV) for t in xwb) for xwb in ins]
+    ys = [torch.empty(128, 1024, dtype=torch.float16, device=DEV) for _ in range(2)]
+    torch.cuda.synchronize()
+    rcs = [None, None]
+
+    def work(i):
+        x, w, b = dev[i]
+        for _ in range(5):
+            rc = L.poot_linear_f16(x.data_ptr(), w.data_ptr(), b.data_ptr(), ys[i].data_ptr(), 128, 1024, 8192,
+                                   PER_THREAD)
+            if rc != L.POOT_OK:
+                break
+        rcs[i] = rc
+
+    th = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    torch.cuda.synchronize()
+    assert rcs == [L.POOT_OK, L.POOT_OK]
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    for i in range(2):
+        _check(*ins[i], _bits(ys[i]), exact_ints=True)
