@@ -134,7 +134,8 @@ typedef struct poot_linear_options {
                                 width: a multiple of 32 in [64, 256] */
     int gemm_group_m;        /* 0 = automatic; else the number of 128-row
                                 blocks walked together for L2 reuse (>= 1) */
-    int gemm_k_chunk;        /* 0 = automatic (1024); else a multiple of 64:
+    int gemm_k_chunk;        /* 0 = automatic (1024; 2048 for contractions
+                                with epilogue steps); else a multiple of 64:
                                 how many K elements the tensor core sums
                                 before the partial sums are added, in IEEE
                                 FP32, into the running sum.  A value >= K
