@@ -259,9 +259,11 @@ typedef struct poot_contraction_spec {
  * y = the widened contraction of x [M,K] and W [N,K] ([out, in], read in
  * place) with the optional bias b [N] (NULL: none) under `spec`, on
  * `stream`.  All pointers are device pointers; y is [M,N] row-major.
- * Runs on the tcgen05 GEMM for every M (the GEMV kernels serve only
- * poot_linear_f16).  `opts` may be NULL; its GEMV fields and variants are
- * ignored except the GEMM ones.  Asynchronous; the caller owns every
+ * M <= 16 with x and W 16-byte aligned and K % 8 == 0 runs on the GEMV
+ * kernels (a per-element epilogue; the grouped form and a requested split
+ * excepted); everything else on the tcgen05 GEMM.  `opts` may be NULL; of
+ * its variants POOT_VARIANT_GEMV (where the GEMV applies) and the GEMM ones
+ * are accepted, and its GEMV warp split is ignored.  Asynchronous; the caller owns every
  * buffer; the library allocates nothing except the workspace described
  * under poot_linear_f16 (split-K, never for the grouped form; the packed
  * copies of x and W when TMA cannot read them in place).

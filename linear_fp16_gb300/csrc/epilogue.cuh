@@ -136,6 +136,48 @@ __device__ __forceinline__ void ep_activation_pairs(uint32_t* v) {
   }
 }
 
+// The widened contraction's epilogue for one output held as an FP32 sum by
+// one lane (the GEMVs, the split-K reduce): y[m, n] (row pitch ldy) gets
+// RN_h(s), then RN_h(t + b[n]), then the steps, every primitive rounded to
+// the head dtype; or, with out_f32, the FP32 sum (+ b[n] in FP32).
+struct ElemEpilogue {
+  int dtype, out_f32, has_bias, num_steps;
+  int op[kEpiMaxSteps];
+  const uint16_t* ptr[kEpiMaxSteps];  // ADD / MUL operands [.., ld]
+  long long ld[kEpiMaxSteps];
+  const uint16_t* b;  // [N] head-dtype bits, or nullptr
+  uint16_t* y;        // head-dtype bits (out_f32 == 0)
+  float* y32;         // out_f32 == 1
+  long long ldy;
+};
+
+// the head value after bias and steps (not yet stored)
+__device__ __forceinline__ float elem_head(const ElemEpilogue& e, float s, int m, int n) {
+  const int dt = e.dtype;
+  float t = ep_rh(s, dt);
+  if (e.has_bias) t = ep_rh(__fadd_rn(t, ep_widen(__ldg(e.b + n), dt)), dt);
+  for (int st = 0; st < e.num_steps; ++st) {
+    const int op = e.op[st];
+    if (op == kEpAdd || op == kEpMul) {
+      const float r = ep_widen(__ldg(e.ptr[st] + (size_t)m * (size_t)e.ld[st] + n), dt);
+      t = ep_rh(op == kEpAdd ? __fadd_rn(t, r) : __fmul_rn(t, r), dt);
+    } else {
+      t = ep_activation(op, t, dt);
+    }
+  }
+  return t;
+}
+
+__device__ __forceinline__ void elem_store(const ElemEpilogue& e, float s, int m, int n) {
+  const size_t i = (size_t)m * (size_t)e.ldy + n;
+  if (e.out_f32) {
+    e.y32[i] = e.has_bias ? __fadd_rn(s, ep_widen(__ldg(e.b + n), e.dtype)) : s;
+    return;
+  }
+  const float t = elem_head(e, s, m, n);
+  e.y[i] = e.dtype == kEpiBf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(t)) : __half_as_ushort(__float2half_rn(t));
+}
+
 // Eight consecutive elements (bits) of row `row`, columns c .. c+7, of an
 // [M, ld] operand; zero outside [M) x [N).  `vec`: base 16-byte aligned and
 // ld % 8 == 0 (c is a multiple of 8), so a full chunk is one 16-byte load.

@@ -15,6 +15,7 @@
 // Graph IR" page (one op; GEMV and GEMM specialised from static shapes).
 #pragma once
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace poot {
@@ -31,6 +32,9 @@ struct GemvArgs {
   int M, N, K;
   int wpr;  // warps per W row: 1, 2, 4 or 8
   int kc;   // K chunk staged in shared memory (multiple of 256)
+  // the widened contraction (WIDE instantiations): x, W, b in the head
+  // dtype, y by the per-element epilogue
+  ElemEpilogue e;
   int prefetch;  // tensor-core GEMV: bulk-prefetch each warp's W slice into L2 first
 };
 
@@ -39,6 +43,18 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// eight binary16 (DT = kEpiF16) or bfloat16 values, widened exactly
+template <int DT>
+__device__ __forceinline__ void unpack8_t(const uint4 v, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = ep_unpack_t<DT>(u[i]);
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
   }
@@ -167,7 +183,9 @@ constexpr int kGemvRowWarps = 4;
 constexpr int kGemvRowThreads = kGemvRowWarps * 32;
 constexpr int kGemvRowVpl = 16;  // vectors per lane per chunk (16 * 32 * 8 = 4096 elements)
 
-template <int MT>
+// DT: the operands' dtype; WIDE: the widened contraction's epilogue
+// (a.e) instead of y = RN16(RN16(sum) + b).
+template <int MT, int DT = kEpiF16, bool WIDE = false>
 __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const GemvArgs a) {
   __shared__ float red[kGemvRowWarps][MT];
   const int warp = threadIdx.x >> 5;
@@ -190,15 +208,15 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
 #pragma unroll
   for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
   // b[row] is fetched now, beside the first W loads, not after the sum
-  const __half bn = (active && part == 0) ? a.b[row] : __float2half_rn(0.0f);
+  const __half bn = (!WIDE && active && part == 0) ? a.b[row] : __float2half_rn(0.0f);
 
   auto fma_vec = [&](const uint4 wvec, int v) {
     float wf[8];
-    unpack8(wvec, wf);
+    unpack8_t<DT>(wvec, wf);
 #pragma unroll
     for (int m = 0; m < MT; ++m) {  // MT == M here (M <= 2)
       float xf[8];
-      unpack8(__ldg(xv + (size_t)m * nvec + v), xf);
+      unpack8_t<DT>(__ldg(xv + (size_t)m * nvec + v), xf);
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[m] = fmaf(wf[j], xf[j], acc[m]);
     }
@@ -256,8 +274,12 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (lane == m && m < a.M) {
-        const __half p = __float2half_rn(acc[m]);  // proj, rounded before the bias
-        a.y[(size_t)m * a.N + row] = __hadd(p, bn);
+        if constexpr (WIDE) {
+          elem_store(a.e, acc[m], m, row);
+        } else {
+          const __half p = __float2half_rn(acc[m]);  // proj, rounded before the bias
+          a.y[(size_t)m * a.N + row] = __hadd(p, bn);
+        }
       }
     }
   }
@@ -293,8 +315,26 @@ __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, ui
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16)
-template <int NT, int WARPS>
+// the same MMA on bfloat16 operands
+__device__ __forceinline__ void mma_16816_bf16_f32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                   uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int DT>
+__device__ __forceinline__ void mma_16816_f32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  if constexpr (DT == kEpiBf16) mma_16816_bf16_f32(d, a0, a1, a2, a3, b0, b1);
+  else mma_16816_f16_f32(d, a0, a1, a2, a3, b0, b1);
+}
+
+// NT = number of 8-column blocks of m (1: M <= 8, 2: M <= 16); DT and WIDE
+// as for gemv_f16_rows_kernel
+template <int NT, int WARPS, int DT = kEpiF16, bool WIDE = false>
 __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs a) {
   __shared__ float red[WARPS][32][4 * NT];
   const int warp = threadIdx.x >> 5;
@@ -321,8 +361,8 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
   grid_dep_wait();
   grid_dep_launch();
   // bias of this lane's two output features, fetched early
-  const float bA = (warp == 0 && okA) ? __half2float(a.b[nA]) : 0.0f;
-  const float bB = (warp == 0 && okB) ? __half2float(a.b[nB]) : 0.0f;
+  const float bA = (!WIDE && warp == 0 && okA) ? __half2float(a.b[nA]) : 0.0f;
+  const float bB = (!WIDE && warp == 0 && okB) ? __half2float(a.b[nB]) : 0.0f;
 
   float d[NT][4];
 #pragma unroll
@@ -345,8 +385,8 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
-        mma_16816_f16_f32(d[q], va[u].x, vb[u].x, va[u].y, vb[u].y, vx[u][q].x, vx[u][q].y);
-        mma_16816_f16_f32(d[q], va[u].z, vb[u].z, va[u].w, vb[u].w, vx[u][q].z, vx[u][q].w);
+        mma_16816_f32<DT>(d[q], va[u].x, vb[u].x, va[u].y, vb[u].y, vx[u][q].x, vx[u][q].y);
+        mma_16816_f32<DT>(d[q], va[u].z, vb[u].z, va[u].w, vb[u].w, vx[u][q].z, vx[u][q].w);
       }
     }
   }
@@ -367,8 +407,12 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
       const int m = 8 * q + 2 * t + (i & 1);
       const int n = (i < 2) ? nA : nB;
       if (m < M && n < N) {
-        const __half p = __float2half_rn(s);  // proj, rounded before the bias
-        a.y[(size_t)m * N + n] = __hadd(p, __float2half_rn(i < 2 ? bA : bB));
+        if constexpr (WIDE) {
+          elem_store(a.e, s, m, n);
+        } else {
+          const __half p = __float2half_rn(s);  // proj, rounded before the bias
+          a.y[(size_t)m * N + n] = __hadd(p, __float2half_rn(i < 2 ? bA : bB));
+        }
       }
     }
   }

@@ -628,18 +628,19 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     ra.S = S;
     ra.M = a.M;
     ra.N = a.N;
-    ra.dtype = a.dtype;
-    ra.out_f32 = a.out_f32;
-    ra.has_bias = a.has_bias;
-    ra.num_steps = a.num_steps;
+    ra.e.dtype = a.dtype;
+    ra.e.out_f32 = a.out_f32;
+    ra.e.has_bias = a.has_bias;
+    ra.e.num_steps = a.num_steps;
     for (int s = 0; s < kEpiMaxSteps; ++s) {
-      ra.ep_op[s] = a.ep_op[s];
-      ra.ep_ptr[s] = a.ep_ptr[s];
-      ra.ep_ld[s] = a.ep_ld[s];
+      ra.e.op[s] = a.ep_op[s];
+      ra.e.ptr[s] = a.ep_ptr[s];
+      ra.e.ld[s] = a.ep_ld[s];
     }
-    ra.b = reinterpret_cast<const uint16_t*>(b);
-    ra.y = a.out_f32 ? nullptr : static_cast<uint16_t*>(y);
-    ra.y32 = a.out_f32 ? static_cast<float*>(y) : nullptr;
+    ra.e.b = reinterpret_cast<const uint16_t*>(b);
+    ra.e.y = a.out_f32 ? nullptr : static_cast<uint16_t*>(y);
+    ra.e.y32 = a.out_f32 ? static_cast<float*>(y) : nullptr;
+    ra.e.ldy = N;
     // the GEMM writes the unrounded partial sums of each split
     a.general = 1;
     a.out_f32 = 1;
@@ -745,7 +746,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     e = full ? launch_widened(std::integral_constant<int, kEpiFull>{})
              : launch_widened(std::integral_constant<int, kEpiHead>{});
     if (e == cudaSuccess && S > 1) {
-      const bool vec = N % 4 == 0 && (ra.out_f32 ? aligned(y, 16) : aligned(y, 8));
+      const bool vec = N % 4 == 0 && (ra.e.out_f32 ? aligned(y, 16) : aligned(y, 8));
       const int64_t units = vec ? M * N / 4 : M * N;
       int64_t blocks = (units + 255) / 256;
       const int64_t cap = int64_t(st.sm_count) * 8;
@@ -817,6 +818,7 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   const int64_t kround = (K + 255) / 256 * 256;
   if (kc > kround) kc = kround;
   GemvArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.x = static_cast<const __half*>(x);
   a.w = static_cast<const __half*>(w);
   a.b = static_cast<const __half*>(b);
@@ -858,6 +860,75 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
     e = launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
   } else {
     e = launch_gemv_mt<false>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
+  }
+  return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+}
+
+// The widened contraction for 1 <= M <= 16 (one group, x and W 16-byte
+// aligned, K % 8 == 0) on the GEMV kernels: the same W stream, the operands
+// in the head dtype, each output through the per-element epilogue.
+int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const void* b, void* y, int64_t M,
+                     int64_t N, int64_t K, const EpiConfig& epi, cudaStream_t stream) {
+  GemvArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = static_cast<const __half*>(x);
+  a.w = static_cast<const __half*>(w);
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.e.dtype = epi.dtype;
+  a.e.out_f32 = epi.out_f32;
+  a.e.has_bias = b != nullptr ? 1 : 0;
+  a.e.num_steps = epi.num_steps;
+  for (int s = 0; s < kEpiMaxSteps; ++s) {
+    const bool used = s < epi.num_steps;
+    a.e.op[s] = used ? epi.op[s] : 0;
+    a.e.ptr[s] = used ? static_cast<const uint16_t*>(epi.ptr[s]) : nullptr;
+    a.e.ld[s] = used ? epi.ld[s] : 0;
+  }
+  a.e.b = static_cast<const uint16_t*>(b);
+  a.e.y = epi.out_f32 ? nullptr : static_cast<uint16_t*>(y);
+  a.e.y32 = epi.out_f32 ? static_cast<float*>(y) : nullptr;
+  a.e.ldy = N;
+  const bool bf = epi.dtype == POOT_DTYPE_BF16;
+  cudaError_t e;
+  if (M <= 2) {
+    // one warp per W row (or per K slice): about 16 warps per SM
+    const int64_t target = int64_t(st.sm_count) * 16;
+    int wpr = 1;
+    while (wpr < kGemvRowWarps && N * wpr < target) wpr *= 2;
+    a.wpr = wpr;
+    const int rpb = kGemvRowWarps / wpr;
+    const dim3 grid(static_cast<unsigned>((N + rpb - 1) / rpb)), block(kGemvRowThreads);
+    if (M == 1)
+      e = bf ? launch(gemv_f16_rows_kernel<1, kEpiBf16, true>, grid, block, 0, stream, a)
+             : launch(gemv_f16_rows_kernel<1, kEpiF16, true>, grid, block, 0, stream, a);
+    else
+      e = bf ? launch(gemv_f16_rows_kernel<2, kEpiBf16, true>, grid, block, 0, stream, a)
+             : launch(gemv_f16_rows_kernel<2, kEpiF16, true>, grid, block, 0, stream, a);
+  } else {
+    // the tensor-core GEMV, with the plain call's warp and prefetch rules
+    const int64_t tiles = (N + 15) / 16;
+    const dim3 grid(static_cast<unsigned>(tiles));
+    const bool few = tiles < 4 * int64_t(st.sm_count);
+    a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
+    constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
+    const dim3 block((few ? WF : WM) * 32);
+    if (M <= 8) {
+      if (bf)
+        e = few ? launch(gemv_f16_mma_kernel<1, WF, kEpiBf16, true>, grid, block, 0, stream, a)
+                : launch(gemv_f16_mma_kernel<1, WM, kEpiBf16, true>, grid, block, 0, stream, a);
+      else
+        e = few ? launch(gemv_f16_mma_kernel<1, WF, kEpiF16, true>, grid, block, 0, stream, a)
+                : launch(gemv_f16_mma_kernel<1, WM, kEpiF16, true>, grid, block, 0, stream, a);
+    } else {
+      if (bf)
+        e = few ? launch(gemv_f16_mma_kernel<2, WF, kEpiBf16, true>, grid, block, 0, stream, a)
+                : launch(gemv_f16_mma_kernel<2, WM, kEpiBf16, true>, grid, block, 0, stream, a);
+      else
+        e = few ? launch(gemv_f16_mma_kernel<2, WF, kEpiF16, true>, grid, block, 0, stream, a)
+                : launch(gemv_f16_mma_kernel<2, WM, kEpiF16, true>, grid, block, 0, stream, a);
+    }
   }
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
@@ -950,8 +1021,9 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
   o.variant = POOT_VARIANT_AUTO;
   if (opts != nullptr) o = *opts;
   if (!gemm_options_ok(o) || o.gemm_cluster == 4) return POOT_ERR_INVALID_ARG;
-  if (o.variant != POOT_VARIANT_AUTO && o.variant != POOT_VARIANT_GEMM_TMA && o.variant != POOT_VARIANT_GEMM_CPASYNC &&
-      o.variant != POOT_VARIANT_GEMM_REG && o.variant != POOT_VARIANT_GEMM_PACKED)
+  if (o.variant != POOT_VARIANT_AUTO && o.variant != POOT_VARIANT_GEMV && o.variant != POOT_VARIANT_GEMM_TMA &&
+      o.variant != POOT_VARIANT_GEMM_CPASYNC && o.variant != POOT_VARIANT_GEMM_REG &&
+      o.variant != POOT_VARIANT_GEMM_PACKED)
     return POOT_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return POOT_OK;
   if (K == 0 || x == nullptr || w == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
@@ -965,6 +1037,17 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
     if (epi.ptr[s] == nullptr) continue;
     if (!aligned(epi.ptr[s], 2)) return POOT_ERR_MISALIGNED;
     if (overlaps(y, ybytes, epi.ptr[s], ((G * M - 1) * epi.ld[s] + N) * 2)) return POOT_ERR_INVALID_ARG;
+  }
+  // M <= 16 (one group, operands readable by 16-byte loads, no GEMM split
+  // asked for): the GEMV kernels with the per-element epilogue
+  const bool gemv_ok = G == 1 && M <= POOT_GEMV_MAX_M && xw_tma_ok(x, w, K);
+  if (o.variant == POOT_VARIANT_GEMV && !gemv_ok) return POOT_ERR_INVALID_ARG;
+  if (o.variant == POOT_VARIANT_GEMV || (o.variant == POOT_VARIANT_AUTO && gemv_ok && o.gemm_split_k <= 1)) {
+    int dev = 0;
+    DeviceState* st = nullptr;
+    const int rc = device_state(&dev, &st);
+    if (rc != POOT_OK) return rc;
+    return launch_gemv_wide(*st, x, w, b, y, M, N, K, epi, stream);
   }
   int variant = o.variant;
   if (variant == POOT_VARIANT_AUTO) {

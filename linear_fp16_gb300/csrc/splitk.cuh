@@ -16,31 +16,8 @@ struct SplitReduceArgs {
   const float* ws;  // [S, M, N] partial sums
   int S;
   int M, N;
-  int dtype, out_f32, has_bias, num_steps;
-  int ep_op[kEpiMaxSteps];
-  const uint16_t* ep_ptr[kEpiMaxSteps];
-  long long ep_ld[kEpiMaxSteps];
-  const uint16_t* b;  // [N] head-dtype bits, or nullptr
-  uint16_t* y;        // [M, N] head-dtype bits (out_f32 == 0)
-  float* y32;         // [M, N] (out_f32 == 1)
+  ElemEpilogue e;   // the contraction's epilogue, y row pitch N
 };
-
-// The epilogue of one element from its FP32 sum s (row m, column n).
-__device__ __forceinline__ float splitk_epilogue(const SplitReduceArgs& a, float s, int m, int n) {
-  const int dt = a.dtype;
-  float t = ep_rh(s, dt);
-  if (a.has_bias) t = ep_rh(__fadd_rn(t, ep_widen(__ldg(a.b + n), dt)), dt);
-  for (int st = 0; st < a.num_steps; ++st) {
-    const int op = a.ep_op[st];
-    if (op == kEpAdd || op == kEpMul) {
-      const float r = ep_widen(__ldg(a.ep_ptr[st] + (size_t)m * (size_t)a.ep_ld[st] + n), dt);
-      t = ep_rh(op == kEpAdd ? __fadd_rn(t, r) : __fmul_rn(t, r), dt);
-    } else {
-      t = ep_activation(op, t, dt);
-    }
-  }
-  return t;
-}
 
 // VEC = 4: four consecutive elements of one row per thread (N % 4 == 0, the
 // workspace 16-byte aligned, y 8-byte / y32 16-byte aligned): one 16-byte
@@ -51,7 +28,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const SplitReduceArg
   grid_dep_launch();
   const long long MN = (long long)a.M * a.N;
   const long long units = MN / VEC;
-  const int dt = a.dtype;
+  const int dt = a.e.dtype;
   for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
        u += (long long)gridDim.x * blockDim.x) {
     const long long i = u * VEC;
@@ -71,24 +48,25 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const SplitReduceArg
       for (int k = 1; k < a.S; ++k) s[0] = __fadd_rn(s[0], __ldg(a.ws + (long long)k * MN + i));
     }
     const int m = (int)(i / a.N), n0 = (int)(i - (long long)m * a.N);
-    if (a.out_f32) {
+    const ElemEpilogue& e = a.e;
+    if (e.out_f32) {
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
-        if (a.has_bias) s[j] = __fadd_rn(s[j], ep_widen(__ldg(a.b + n0 + j), dt));
+        if (e.has_bias) s[j] = __fadd_rn(s[j], ep_widen(__ldg(e.b + n0 + j), dt));
       if constexpr (VEC == 4) {
-        *reinterpret_cast<float4*>(a.y32 + i) = make_float4(s[0], s[1], s[2], s[3]);
+        *reinterpret_cast<float4*>(e.y32 + i) = make_float4(s[0], s[1], s[2], s[3]);
       } else {
-        a.y32[i] = s[0];
+        e.y32[i] = s[0];
       }
       continue;
     }
     float t[VEC];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) t[j] = splitk_epilogue(a, s[j], m, n0 + j);
+    for (int j = 0; j < VEC; ++j) t[j] = elem_head(e, s[j], m, n0 + j);
     if constexpr (VEC == 4) {
-      *reinterpret_cast<uint2*>(a.y + i) = make_uint2(ep_pack(t[0], t[1], dt), ep_pack(t[2], t[3], dt));
+      *reinterpret_cast<uint2*>(e.y + i) = make_uint2(ep_pack(t[0], t[1], dt), ep_pack(t[2], t[3], dt));
     } else {
-      a.y[i] = dt == kEpiBf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(t[0]))
+      e.y[i] = dt == kEpiBf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(t[0]))
                               : __half_as_ushort(__float2half_rn(t[0]));
     }
   }

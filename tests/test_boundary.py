@@ -220,9 +220,16 @@ def test_contract_argument_errors_before_any_cuda_call(spec, args, code):
     assert L.poot_contract(*args, spec, None, 0) == code
 
 
-def test_contract_rejects_clusters_of_four_and_gemv_variants():
+def test_contract_rejects_clusters_of_four_and_inapplicable_gemv_variants():
     assert L.poot_contract(X, W, B, Y, 400, 64, 64, _spec(), L.options(gemm_cluster=4), 0) == L.POOT_ERR_INVALID_ARG
-    assert L.poot_contract(X, W, B, Y, 4, 64, 64, _spec(), L.options(L.VARIANT_GEMV), 0) == L.POOT_ERR_INVALID_ARG
+    # the scalar GEMV never serves the contraction; the vector GEMV only for
+    # M <= 16 with 16-byte aligned x and W and K % 8 == 0
+    assert L.poot_contract(X, W, B, Y, 4, 64, 64, _spec(), L.options(L.VARIANT_GEMV_SCALAR), 0) == \
+        L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(X, W, B, Y, 17, 64, 64, _spec(), L.options(L.VARIANT_GEMV), 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(X, W, B, Y, 4, 64, 66, _spec(), L.options(L.VARIANT_GEMV), 0) == L.POOT_ERR_INVALID_ARG
+    assert L.poot_contract(X + 2, W, B, Y, 4, 64, 64, _spec(), L.options(L.VARIANT_GEMV), 0) == \
+        L.POOT_ERR_INVALID_ARG
 
 
 def test_contract_null_spec_and_empty_problems():

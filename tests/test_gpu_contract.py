@@ -274,11 +274,15 @@ def test_strided_and_unaligned_operands():
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 512), (8, 1000, 770), (16, 72, 33)])
-def test_small_m_runs_on_the_gemm(M, N, K):
+def test_small_m_on_the_gemv_and_the_gemm(M, N, K):
+    # K % 8 == 0: the GEMV with the per-element epilogue; else (and when the
+    # GEMM is forced) the tcgen05 GEMM with M rows of its 128-row tile
     x, w, b = _inputs(M, N, K, "smallint", 370 + K, "f16")
     r = _operand(M, N, "smallint", 371, "f16")
     steps = [("mul", r), "silu"]
     _check_head(x, w, b, steps, _gpu(x, w, b, steps=steps), "f16", exact_sums=True)
+    _check_head(x, w, b, steps, _gpu(x, w, b, steps=steps, variant=L.VARIANT_GEMM_PACKED), "f16",
+                exact_sums=True)
 
 
 def test_large_swiglu_sampled_rows():
