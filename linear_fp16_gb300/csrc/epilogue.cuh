@@ -151,11 +151,12 @@ struct ElemEpilogue {
   long long ldy;
 };
 
-// the head value after bias and steps (not yet stored)
-__device__ __forceinline__ float elem_head(const ElemEpilogue& e, float s, int m, int n) {
+// the head value after bias and steps (not yet stored); output row m and
+// column n, bias element nb (n, or group * N + n for a grouped contraction)
+__device__ __forceinline__ float elem_head(const ElemEpilogue& e, float s, int m, int n, int nb) {
   const int dt = e.dtype;
   float t = ep_rh(s, dt);
-  if (e.has_bias) t = ep_rh(__fadd_rn(t, ep_widen(__ldg(e.b + n), dt)), dt);
+  if (e.has_bias) t = ep_rh(__fadd_rn(t, ep_widen(__ldg(e.b + nb), dt)), dt);
   for (int st = 0; st < e.num_steps; ++st) {
     const int op = e.op[st];
     if (op == kEpAdd || op == kEpMul) {
@@ -168,13 +169,13 @@ __device__ __forceinline__ float elem_head(const ElemEpilogue& e, float s, int m
   return t;
 }
 
-__device__ __forceinline__ void elem_store(const ElemEpilogue& e, float s, int m, int n) {
+__device__ __forceinline__ void elem_store(const ElemEpilogue& e, float s, int m, int n, int nb) {
   const size_t i = (size_t)m * (size_t)e.ldy + n;
   if (e.out_f32) {
-    e.y32[i] = e.has_bias ? __fadd_rn(s, ep_widen(__ldg(e.b + n), e.dtype)) : s;
+    e.y32[i] = e.has_bias ? __fadd_rn(s, ep_widen(__ldg(e.b + nb), e.dtype)) : s;
     return;
   }
-  const float t = elem_head(e, s, m, n);
+  const float t = elem_head(e, s, m, n, nb);
   e.y[i] = e.dtype == kEpiBf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(t)) : __half_as_ushort(__float2half_rn(t));
 }
 

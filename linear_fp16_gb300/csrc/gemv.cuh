@@ -33,8 +33,11 @@ struct GemvArgs {
   int wpr;  // warps per W row: 1, 2, 4 or 8
   int kc;   // K chunk staged in shared memory (multiple of 256)
   // the widened contraction (WIDE instantiations): x, W, b in the head
-  // dtype, y by the per-element epilogue
+  // dtype, y by the per-element epilogue; `groups` independent contractions
+  // (x [groups*M, K], W [groups*N, K], y and step operands [groups*M, ..],
+  // b [groups*N]); 1 on the plain path
   ElemEpilogue e;
+  int groups;
   int prefetch;  // tensor-core GEMV: bulk-prefetch each warp's W slice into L2 first
 };
 
@@ -191,9 +194,11 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wpr = a.wpr;
-  const int row = blockIdx.x * (kGemvRowWarps / wpr) + warp / wpr;
+  const int row = blockIdx.x * (kGemvRowWarps / wpr) + warp / wpr;  // W row, over all groups
   const int part = warp % wpr;
-  const bool active = row < a.N;
+  const bool active = row < a.N * a.groups;
+  const int grp = WIDE ? row / a.N : 0;  // this row's group and column in it
+  const int col = row - grp * a.N;
   const int nvec = a.K >> 3;
   // this warp's contiguous slice of the row, in whole chunks of 32 vectors
   const int segs = (nvec + 31) >> 5;
@@ -201,7 +206,8 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
   const int v_begin = min(nvec, part * seg_per_part * 32);
   const int v_end = min(nvec, (part + 1) * seg_per_part * 32);
   const uint4* __restrict__ wv = reinterpret_cast<const uint4*>(a.w + (size_t)(active ? row : 0) * a.K);
-  const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(a.x);
+  const uint4* __restrict__ xv =
+      reinterpret_cast<const uint4*>(a.x + (size_t)(active ? grp : 0) * (size_t)a.M * a.K);
   grid_dep_wait();
 
   float acc[MT];
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
     for (int m = 0; m < MT; ++m) {
       if (lane == m && m < a.M) {
         if constexpr (WIDE) {
-          elem_store(a.e, acc[m], m, row);
+          elem_store(a.e, acc[m], grp * a.M + m, col, row);
         } else {
           const __half p = __float2half_rn(acc[m]);  // proj, rounded before the bias
           a.y[(size_t)m * a.N + row] = __hadd(p, bn);
@@ -340,8 +346,14 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int n0 = blockIdx.x * 16;
   const int K = a.K, N = a.N, M = a.M;
+  // WIDE: 16-row tiles of W per group (a tile never spans two groups)
+  int grp = 0, n0 = blockIdx.x * 16;
+  if constexpr (WIDE) {
+    const int tpg = (N + 15) / 16;
+    grp = (int)blockIdx.x / tpg;
+    n0 = ((int)blockIdx.x - grp * tpg) * 16;
+  }
   const int nA = n0 + g, nB = n0 + g + 8;
   // this warp's K slice, a multiple of 32
   const int slice = ((K + WARPS * 32 - 1) / (WARPS * 32)) * 32;
@@ -351,6 +363,13 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
   const __half* __restrict__ wb = a.w + (size_t)(nB < N ? nB : 0) * K;
   const __half* __restrict__ x0 = a.x + (size_t)(g < M ? g : 0) * K;
   const __half* __restrict__ x1 = a.x + (size_t)(g + 8 < M ? g + 8 : 0) * K;
+  if constexpr (WIDE) {
+    // this group's W rows and x rows
+    wa += (size_t)grp * N * K;
+    wb += (size_t)grp * N * K;
+    x0 += (size_t)grp * M * K;
+    x1 += (size_t)grp * M * K;
+  }
   const bool okA = nA < N, okB = nB < N, okx0 = g < M, okx1 = (NT > 1) && (g + 8 < M);
   // start this warp's K slice of its 16 W rows towards L2 while the
   // previous grid drains (lane 4g prefetches rows nA and nB)
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_f16_mma_kernel(const GemvArgs
       const int n = (i < 2) ? nA : nB;
       if (m < M && n < N) {
         if constexpr (WIDE) {
-          elem_store(a.e, s, m, n);
+          elem_store(a.e, s, grp * M + m, n, grp * N + n);
         } else {
           const __half p = __float2half_rn(s);  // proj, rounded before the bias
           a.y[(size_t)m * N + n] = __hadd(p, __float2half_rn(i < 2 ? bA : bB));

@@ -828,6 +828,7 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   a.K = static_cast<int>(K);
   a.wpr = wpr;
   a.kc = static_cast<int>(kc);
+  a.groups = 1;
   a.prefetch = 0;
   const int rows_per_block = kGemvWarps / wpr;
   const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
@@ -864,13 +865,14 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
 }
 
-// The widened contraction for 1 <= M <= 16 (one group, x and W 16-byte
-// aligned, K % 8 == 0) on the GEMV kernels: the same W stream, the operands
-// in the head dtype, each output through the per-element epilogue.
+// The widened contraction for 1 <= M <= 16 (x and W 16-byte aligned,
+// K % 8 == 0; G groups) on the GEMV kernels: the same W stream, the
+// operands in the head dtype, each output through the per-element epilogue.
 int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const void* b, void* y, int64_t M,
-                     int64_t N, int64_t K, const EpiConfig& epi, cudaStream_t stream) {
+                     int64_t N, int64_t K, int64_t G, const EpiConfig& epi, cudaStream_t stream) {
   GemvArgs a;
   std::memset(&a, 0, sizeof(a));
+  a.groups = static_cast<int>(G);
   a.x = static_cast<const __half*>(x);
   a.w = static_cast<const __half*>(w);
   a.M = static_cast<int>(M);
@@ -896,10 +898,10 @@ int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const 
     // one warp per W row (or per K slice): about 16 warps per SM
     const int64_t target = int64_t(st.sm_count) * 16;
     int wpr = 1;
-    while (wpr < kGemvRowWarps && N * wpr < target) wpr *= 2;
+    while (wpr < kGemvRowWarps && G * N * wpr < target) wpr *= 2;
     a.wpr = wpr;
     const int rpb = kGemvRowWarps / wpr;
-    const dim3 grid(static_cast<unsigned>((N + rpb - 1) / rpb)), block(kGemvRowThreads);
+    const dim3 grid(static_cast<unsigned>((G * N + rpb - 1) / rpb)), block(kGemvRowThreads);
     if (M == 1)
       e = bf ? launch(gemv_f16_rows_kernel<1, kEpiBf16, true>, grid, block, 0, stream, a)
              : launch(gemv_f16_rows_kernel<1, kEpiF16, true>, grid, block, 0, stream, a);
@@ -908,7 +910,8 @@ int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const 
              : launch(gemv_f16_rows_kernel<2, kEpiF16, true>, grid, block, 0, stream, a);
   } else {
     // the tensor-core GEMV, with the plain call's warp and prefetch rules
-    const int64_t tiles = (N + 15) / 16;
+    // (16-row tiles per group)
+    const int64_t tiles = G * ((N + 15) / 16);
     const dim3 grid(static_cast<unsigned>(tiles));
     const bool few = tiles < 4 * int64_t(st.sm_count);
     a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
@@ -1038,16 +1041,16 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
     if (!aligned(epi.ptr[s], 2)) return POOT_ERR_MISALIGNED;
     if (overlaps(y, ybytes, epi.ptr[s], ((G * M - 1) * epi.ld[s] + N) * 2)) return POOT_ERR_INVALID_ARG;
   }
-  // M <= 16 (one group, operands readable by 16-byte loads, no GEMM split
-  // asked for): the GEMV kernels with the per-element epilogue
-  const bool gemv_ok = G == 1 && M <= POOT_GEMV_MAX_M && xw_tma_ok(x, w, K);
+  // M <= 16 (operands readable by 16-byte loads, no GEMM split asked for):
+  // the GEMV kernels with the per-element epilogue, any number of groups
+  const bool gemv_ok = M <= POOT_GEMV_MAX_M && xw_tma_ok(x, w, K);
   if (o.variant == POOT_VARIANT_GEMV && !gemv_ok) return POOT_ERR_INVALID_ARG;
   if (o.variant == POOT_VARIANT_GEMV || (o.variant == POOT_VARIANT_AUTO && gemv_ok && o.gemm_split_k <= 1)) {
     int dev = 0;
     DeviceState* st = nullptr;
     const int rc = device_state(&dev, &st);
     if (rc != POOT_OK) return rc;
-    return launch_gemv_wide(*st, x, w, b, y, M, N, K, epi, stream);
+    return launch_gemv_wide(*st, x, w, b, y, M, N, K, G, epi, stream);
   }
   int variant = o.variant;
   if (variant == POOT_VARIANT_AUTO) {

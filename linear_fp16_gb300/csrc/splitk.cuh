@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const SplitReduceArg
     }
     float t[VEC];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) t[j] = elem_head(e, s[j], m, n0 + j);
+    for (int j = 0; j < VEC; ++j) t[j] = elem_head(e, s[j], m, n0 + j, n0 + j);
     if constexpr (VEC == 4) {
       *reinterpret_cast<uint2*>(e.y + i) = make_uint2(ep_pack(t[0], t[1], dt), ep_pack(t[2], t[3], dt));
     } else {

@@ -73,3 +73,27 @@ def test_gemv_variant_refused_where_it_does_not_apply():
     x, w, b = _inputs(4, 64, 66, "smallint", 1601, "f16")
     with pytest.raises(L.PootLinearError):
         _gpu(x, w, b, variant=L.VARIANT_GEMV)   # K % 8 != 0
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("G,M", [(3, 1), (4, 2), (2, 8), (5, 16)])
+def test_grouped_gemv_exact(dt, G, M):
+    # small M per group (one token per expert and the like) on the GEMV,
+    # against the grouped GEMM bit for bit and the oracle per group
+    N, K = 264, 512
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    gen = torch.Generator().manual_seed(1700 + G * 31 + M)
+    x = torch.randint(-4, 5, (G, M, K), generator=gen).to(tdt)
+    w = torch.randint(-4, 5, (G * N, K), generator=gen).to(tdt)
+    b = torch.randint(-4, 5, (G * N,), generator=gen).to(tdt)
+    r = torch.randint(-4, 5, (G, M, N), generator=gen).to(tdt)
+    dev = "cuda:0"
+    steps = ["silu", ("mul", r.to(dev))]
+    y = L.contract(x.to(dev), w.to(dev), b.to(dev), steps=steps)
+    y_gemm = L.contract(x.to(dev), w.to(dev), b.to(dev), steps=steps, variant=L.VARIANT_GEMM_TMA)
+    torch.cuda.synchronize()
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    assert torch.equal(y.view(torch.int16), y_gemm.view(torch.int16))
+    for g in range(G):
+        _check_head(x[g], w[g * N:(g + 1) * N], b[g * N:(g + 1) * N], ["silu", ("mul", r[g])], y[g].cpu(), dt,
+                    exact_sums=True)
