@@ -259,9 +259,9 @@ typedef struct poot_contraction_spec {
  * y = the widened contraction of x [M,K] and W [N,K] ([out, in], read in
  * place) with the optional bias b [N] (NULL: none) under `spec`, on
  * `stream`.  All pointers are device pointers; y is [M,N] row-major.
- * M <= 16 with x and W 16-byte aligned and K % 8 == 0 runs on the GEMV
- * kernels (a per-element epilogue; the grouped form and a requested split
- * excepted); everything else on the tcgen05 GEMM.  `opts` may be NULL; of
+ * M <= 16 (per group) with x and W 16-byte aligned and K % 8 == 0 runs on
+ * the GEMV kernels with a per-element epilogue (unless a GEMM split is
+ * requested); everything else on the tcgen05 GEMM.  `opts` may be NULL; of
  * its variants POOT_VARIANT_GEMV (where the GEMV applies) and the GEMM ones
  * are accepted, and its GEMV warp split is ignored.  Asynchronous; the caller owns every
  * buffer; the library allocates nothing except the workspace described
