@@ -646,6 +646,19 @@ def run_contract(args, rank, world, local):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (step_ms * 1e-3) / 1e12
     alg_bytes = 2 * (M * K + G * N * K + (G * N if with_bias else 0)) + ybytes * M * N + 2 * M * N * n_ops
+    if M // G <= L.GEMV_MAX_M:
+        # M <= 16 per group: the widened GEMV, bound by the W stream
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        gbs = alg_bytes / (step_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": f"{src} STREAM-style copy", "traffic": None,
+                "kernel": "gemv_f16_rows_kernel<wide>" if M // G <= 2 else "gemv_f16_mma_kernel<wide>",
+                "kernel_ms": step_ms, "algorithmic_per_launch": alg_bytes}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{src} dense bf16 burst",
+                "traffic": None, "kernel": "gemm_f16_tcgen05_kernel<tma, widened>",
+                "kernel_ms": step_ms, "algorithmic_per_launch": flops}
     line = {
         "metric": METRIC, "value": world * achieved, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -656,10 +669,7 @@ def run_contract(args, rank, world, local):
                    "l2": "inputs larger than L2" if copies == 1 else f"{copies} rotating copies",
                    "timing": "CUDA graph of the K steps, replayed between two events",
                    "hbm_gbs_algorithmic": alg_bytes / (step_ms * 1e-3) / 1e9},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{src} dense bf16 burst",
-                     "traffic": None, "kernel": "gemm_f16_tcgen05_kernel<tma, general>",
-                     "kernel_ms": step_ms, "algorithmic_per_launch": flops},
+        "roofline": roof,
         "cpu_baseline": None,
         "e2e": None,
         "gpu_launches": args.steps,
