@@ -1,6 +1,6 @@
 """Parity of the widened contraction (poot_contract) with the oracle, on a GPU.
 
-Rules (readings of the pages):
+Rules (the readings of the source pages on the widened contraction):
 * small-integer inputs make every sum exact, so the head value is the
   oracle's; bias, ADD and MUL steps are then bit-exact, and activation steps
   may differ only where FP32 expf / erff and the oracle's binary64 exp / erf
