@@ -263,6 +263,9 @@ def contract(x, w, b=None, out=None, *, out_f32: bool = False, steps=(), gemm_ti
     "silu", "gelu_tanh", "gelu_erf" or ("add" | "mul", r) with r an [M,N]
     tensor (row pitch from its stride) of the head dtype.  Returns y [M,N]:
     float32 with ``out_f32`` (no steps then), else the head dtype.
+    M <= 16 (per group) runs on the GEMV kernels, larger M on the GEMM;
+    ``variant`` may force VARIANT_GEMV or a GEMM variant, and the gemm_*
+    knobs tune the GEMM (``gemm_split_k``: see include/poot_linear.h).
     """
     import torch
     dt = x.dtype
