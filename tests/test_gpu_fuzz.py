@@ -102,3 +102,28 @@ def test_random_contraction_exact(case):
     torch.cuda.synchronize()
     assert L.poot_linear_device_status(0) == L.POOT_OK
     _check_head(x, w, b, host_steps, y.cpu(), dt, exact_sums=True)
+
+
+@pytest.mark.parametrize("case", range(CASES // 2))
+def test_random_linear_normal(case):
+    # normal inputs: the 2-ulp rule of the contract, each output beyond it
+    # inside the FP32-accumulation interval (tests.parity)
+    from tests.parity import compare, legal_interval
+    rng = np.random.default_rng(9000 + case)
+    M, N, K, (ox, ow, oy) = _draw(rng)
+    x, w, b = synth.make_inputs(M, N, K, "normal", 9100 + case)
+    xd, wd, bd = _on_device(x, ox), _on_device(w, ow), b.to(DEV)
+    ybuf = torch.full((M * N + oy + 8,), float("nan"), dtype=torch.float16, device=DEV)
+    yd = ybuf[oy:oy + M * N].view(M, N)
+    L.linear(xd, wd, bd, yd)
+    torch.cuda.synchronize()
+    assert L.poot_linear_device_status(0) == L.POOT_OK
+    got = _bits(yd)
+    yr, pr = oracle.linear_f16(_bits(x), _bits(w), _bits(b), want_proj=True)
+    interval = legal_interval(x.numpy(), w.numpy(), b.numpy())
+    # every output beyond 2 ulps must lie inside the FP32-accumulation
+    # interval; a case of a few ten thousand outputs may hold a handful
+    # (the large-workload tests keep the 1e-5 fraction)
+    ok, rep = compare(got, yr, pr, exact=False, interval=interval, max_outside=max(1e-5, 4.0 / got.size))
+    print(rep)
+    assert ok, rep
