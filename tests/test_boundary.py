@@ -254,3 +254,31 @@ def test_grouped_argument_errors():
     assert L.poot_contract_grouped(X, W, B, W - 3 * 4 * 4 * 2 + 2, 3, 4, 4, 4, sp, None, 0) == \
         L.POOT_ERR_INVALID_ARG
     assert L.poot_contract_grouped(0, 0, 0, 0, 3, 0, 4, 4, sp, None, 0) == L.POOT_OK
+
+
+def _header_constants():
+    """Every `NAME = value` enumerator and `#define NAME value` of the header."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    vals = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(POOT_[A-Z0-9_]+)\s*=\s*(-?\d+)", src)}
+    for m in re.finditer(r"#define\s+(POOT_[A-Z0-9_]+)\s+\(?(-?\d+)\)?\s*$", src, flags=re.M):
+        vals[m.group(1)] = int(m.group(2))
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    vals = _header_constants()
+    mirrors = {name: name[len("POOT_"):] for name in vals}
+    mirrors.update({n: n for n in vals if n.startswith("POOT_OK") or n.startswith("POOT_ERR_")})
+    checked = 0
+    for cname, pyname in mirrors.items():
+        if hasattr(binding, pyname):
+            assert getattr(binding, pyname) == vals[cname], (cname, pyname)
+            checked += 1
+    # every status, variant, dtype and step code, and the two size constants
+    for cname in vals:
+        if cname.startswith(("POOT_ERR_", "POOT_VARIANT_", "POOT_DTYPE_", "POOT_EP_")) or cname == "POOT_OK":
+            assert hasattr(binding, mirrors[cname]), cname
+    assert binding.GEMV_MAX_M == vals["POOT_GEMV_MAX_M"]
+    assert binding.EPILOGUE_MAX_STEPS == vals["POOT_EPILOGUE_MAX_STEPS"]
+    assert checked == len(vals)  # every enumerator and size constant has its mirror
