@@ -142,9 +142,9 @@ typedef struct poot_linear_options {
                                 keeps the whole sum on the tensor core */
     int gemm_cluster;        /* 0 = automatic; 1 = one CTA per 128-row tile;
                                 2 = CTA pairs sharing each W tile on 256-row
-                                tiles (2-SM MMA); 4 = two such pairs on
-                                neighbouring N tiles sharing the x tile.
-                                2 and 4 need the GEMM_TMA variant */
+                                tiles (2-SM MMA); needs the GEMM_TMA or
+                                GEMM_PACKED variant.  Any other value is
+                                POOT_ERR_INVALID_ARG */
     int gemm_split_k;        /* 0 = automatic; 1 = never; S in [2, 16] = cut
                                 the K range into S ranges of whole 64-element
                                 blocks (S must divide ceil(K / 64)), each
@@ -156,7 +156,7 @@ typedef struct poot_linear_options {
                                 for the life of the process; under stream
                                 capture, a graph-owned allocation freed on
                                 the stream after the second kernel.  Not with
-                                gemm_cluster 4, nor with grouped contractions.
+                                grouped contractions.
                                 Automatic splitting happens when one wave of
                                 output tiles leaves more than a quarter of
                                 the SMs idle and K is at least 1024; the tile

@@ -52,9 +52,9 @@ struct GemmArgs {
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int tma_store;  // 1: TMA store of y; 0: plain stores (any pitch/alignment)
   // 1: stages are filled, consumed and released in pairs, and a chunk's last
-  // pair is released through the chunk-complete barrier (TMA producer,
-  // clusters of at most two, even `stages`, every chunk an even number of at
-  // least `stages` K blocks); 0: one stage at a time
+  // pair is released through the chunk-complete barrier (TMA producer, even
+  // `stages`, every chunk an even number of at least `stages` K blocks);
+  // 0: one stage at a time
   int paired;
   // The widened contraction (poot_contract).  general == 0: the plain
   // binary16 epilogue y = RN16(RN16(sum) + b).  general == 1: head dtype
@@ -250,11 +250,6 @@ __device__ __forceinline__ void gemm_copy_rows_cp(uint32_t dst_base, const __hal
 // barriers, and both CTAs' epilogue warps release chunk buffers on the even
 // CTA's "cempty" barriers.  Per SM a stage holds 32 KB instead of 48 KB
 // (BN = 256), so the ring is six stages deep, and W is read once per pair.
-// CL = 4: two pairs on adjacent N tiles of the same 256 rows.  CTAs r and
-// r ^ 2 need the same x rows: each loads half of them and multicasts it to
-// both, so a CTA reads 24 KB per stage from L2 instead of 32 KB.  A stage is
-// refilled only after both pairs' MMAs released it (each "empty" barrier
-// counts one multicast commit from each pair).
 // EPI selects the epilogue compiled in: kEpiPlain, the plain binary16
 // y = RN16(RN16(sum) + b) (the kernel ignores the fields that select the
 // rest); kEpiHead, the widened contraction's head dtype and optional bias
@@ -269,7 +264,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   constexpr bool PAIR = CL >= 2;
   constexpr bool GEN = EPI != kEpiPlain;  // the widened contraction's fields are read
   constexpr bool FULL = EPI == kEpiFull;  // FP32 output, steps, split-K partial sums
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
+  static_assert(CL == 1 || CL == 2, "one CTA or a CTA pair");
   static_assert(!PAIR || MODE == kLoadTma, "the CTA-pair kernel loads through TMA only");
   using L = GemmLayout;
   const int BN = args.bn;
@@ -280,7 +275,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                          ((GEN && args.dtype == kEpiBf16) ? ((1u << 7) | (1u << 10)) : 0u);
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
   const uint32_t rank = crank & 1u;               // row half of the pair's tile
-  const uint32_t pair_id = crank >> 1;            // CL = 4: which of the two N tiles
   const uint32_t lead_rank = crank & ~1u;         // even CTA of this pair
   const bool leader = (rank == 0);
   const int unit = (int)(blockIdx.x / CL);        // cluster (or CTA) index
@@ -322,7 +316,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), MODE == kLoadTma ? 1u : (uint32_t)kGemmCopyThreads);
-      mbar_init(bar_empty(s), CL == 4 ? 2u : 1u);
+      mbar_init(bar_empty(s), 1u);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_cfull(a), 1u);
@@ -370,13 +364,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         // of chunk ch reuses the pair of chunk ch - 1's end).  ck: position
         // in the chunk; ch: chunk count over this CTA's tiles (TMEM buffer and
         // barrier phase).
-        const bool paired = CL <= 2 && args.paired != 0;
+        const bool paired = args.paired != 0;
         const int step = paired ? 2 : 1;
         int ck = 0, ch = 0;
         for (int t = unit; t < args.num_tiles && ok; t += units) {
           int g, mb, nb;
           tile_decode(t, g, mb, nb);
-          if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;  // this pair's N tile
           // rows of this group in the flattened x [groups*M, K] and W [groups*N, K]
           // (a tile that overhangs its group reads rows of the next one; they
           // only reach output rows or columns that are never stored)
@@ -405,14 +398,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 const uint32_t fb0 = map_to_cta(fb, lead_rank);
                 if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
                 const int arow = xrow0 + mb * tile_rows + (int)rank * kGemmBM;
-                if constexpr (CL == 4) {
-                  // half of the x tile, into this CTA and its counterpart in the other pair
-                  const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
-                  tma_load_2d_pair_multicast(stage_a(st) + pair_id * (kGemmBM / 2) * 128u, &tm_x, fb0, kc,
-                                             arow + (int)pair_id * (kGemmBM / 2), mask);
-                } else {
-                  tma_load_2d_pair(stage_a(st), &tm_x, fb0, kc, arow);
-                }
+                tma_load_2d_pair(stage_a(st), &tm_x, fb0, kc, arow);
                 tma_load_2d_pair(stage_b(st), &tm_w, fb0, kc, wrow0 + nb * BN + (int)rank * (BN / 2));
               } else {
                 mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
@@ -499,7 +485,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   } else if (warp == kGemmMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      const bool paired = MODE == kLoadTma && CL <= 2 && args.paired != 0;
+      const bool paired = MODE == kLoadTma && args.paired != 0;
       if (paired) {
         // Two K blocks (two stages, eight MMAs) per iteration over all of
         // this CTA's tiles, one commit each, every tcgen05 instruction
@@ -574,9 +560,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                   umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
               }
               // frees the stage (in both CTAs of a pair) when these MMAs finish
-              // (with CL = 4 in all four CTAs: a stage is refilled by both pairs)
-              if constexpr (CL == 4) umma_commit_pair(bar_empty(stage), 0xF);
-              else if constexpr (PAIR) umma_commit_pair(bar_empty(stage), 3);
+              if constexpr (PAIR) umma_commit_pair(bar_empty(stage), 3);
               else umma_commit(bar_empty(stage));
               if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -611,7 +595,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     for (int t = unit; t < args.num_tiles && ok; t += units) {
       int grp, mb, nb;
       tile_decode(t, grp, mb, nb);
-      if constexpr (CL == 4) nb = 2 * nb + (int)pair_id;
       const int m0 = mb * tile_rows + (int)rank * kGemmBM, n0 = nb * BN;
       // pull this warp's bias values into L1 now, so that the final epilogue
       // reads them at L1 latency instead of waiting on memory once per box

@@ -52,7 +52,6 @@ struct DeviceState {
   int status = POOT_OK;  // POOT_OK or POOT_ERR_UNSUPPORTED_DEVICE / CUDA
   int dev = 0;
   int sm_count = 0;
-  int max_clusters4 = 0;  // co-resident 4-CTA clusters of the GEMM kernel
 };
 
 std::mutex g_mu;
@@ -69,25 +68,6 @@ template <int MODE, int CL, int EPI = kEpiPlain>
 cudaError_t set_gemm_attrs() {
   return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout::DYN_BYTES);
-}
-
-// How many 4-CTA clusters of the GEMM fit on the device at once (clusters
-// live inside one GPC, so this can be less than SMs / 4).
-cudaError_t query_max_clusters4(int* out) {
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(4);
-  cfg.blockDim = dim3(gemm_threads(kLoadTma));
-  cfg.dynamicSmemBytes = Layout::DYN_BYTES;
-  cudaLaunchAttribute attr[1];
-  std::memset(attr, 0, sizeof(attr));
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 4;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, gemm_f16_tcgen05_kernel<kLoadTma, 4>, &cfg);
 }
 
 template <int MT, bool VEC>
@@ -124,7 +104,6 @@ int device_state(int* dev_out, DeviceState** st_out) {
         g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
       }
       if ((e = set_gemm_attrs<kLoadTma, 1>()) != cudaSuccess || (e = set_gemm_attrs<kLoadTma, 2>()) != cudaSuccess ||
-          (e = set_gemm_attrs<kLoadTma, 4>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadCpAsync4, 1>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadReg16, 1>()) != cudaSuccess ||
           (e = set_gemm_attrs<kLoadTma, 1, kEpiHead>()) != cudaSuccess ||
@@ -144,9 +123,6 @@ int device_state(int* dev_out, DeviceState** st_out) {
           (e = set_gemv_attrs<8, false>()) != cudaSuccess ||
           (e = set_gemv_attrs<16, false>()) != cudaSuccess)
         return cuda_fail(e);
-      int mc4 = 0;
-      if ((e = query_max_clusters4(&mc4)) != cudaSuccess) return cuda_fail(e);
-      st.max_clusters4 = mc4;
       st.dev = dev;
       st.sm_count = sms;
       st.status = POOT_OK;
@@ -291,8 +267,8 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 struct GemmPlan {
   int bn, stages, group_m, chunk_kb;
-  int cluster;  // 1: single CTAs; 2: CTA pairs (2-SM MMA); 4: two pairs sharing x
-  bool pair;    // cluster >= 2 (256-row tiles)
+  int cluster;  // 1: single CTAs; 2: CTA pairs (2-SM MMA)
+  bool pair;    // cluster == 2 (256-row tiles)
   int split;    // K ranges (split-K); 1 = none
 };
 
@@ -303,14 +279,11 @@ struct GemmPlan {
 // 128 B/cycle.  The efficiencies of narrower tiles (more x re-reads, more
 // epilogue work per FLOP) were measured on GB300 for 224 (0.90 - 0.97) and
 // extrapolated below it.  Ties go to the wider tile.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, int bn_req, int group_req,
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int bn_req, int group_req,
                    int chunk_req, int cluster_req, int split_req, bool allow_split, bool tma) {
   // CTA pairs (2-SM MMA) from M = 256 (one full pair tile); single CTAs
   // when M is smaller, for short K in one wave, or when the operands need
   // copies.
-  // Clusters of two pairs sharing the x tile cut L2 reads by a fifth but fit
-  // only 36 clusters (144 SMs); interleaved timing on GB300 showed no gain
-  // over pairs on 4096^3 and 8192x14336x4096, so they are opt-in.
   int cluster = 1;
   bool short_k_wave = false;
   if (tma) {
@@ -328,7 +301,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int max_clusters4, 
   }
   const bool pair = cluster >= 2;
   const int64_t bm = pair ? 2 * kGemmBM : kGemmBM;
-  const int64_t slots = cluster == 4 ? 2 * int64_t(max_clusters4) : pair ? sms / 2 : sms;
+  const int64_t slots = pair ? sms / 2 : sms;
   const int64_t num_m = (M + bm - 1) / bm;
   const int64_t num_kb = (K + kGemmBK - 1) / kGemmBK;
   int best_bn = 256;
@@ -534,7 +507,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   const bool packed = variant == POOT_VARIANT_GEMM_PACKED;
   if (packed && fixed_ws != nullptr) return POOT_ERR_INVALID_ARG;
   if (packed) variant = POOT_VARIANT_GEMM_TMA;
-  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, st.max_clusters4, bn_req, group_req, chunk_req,
+  const GemmPlan plan = plan_gemm(M, N, K, st.sm_count, bn_req, group_req, chunk_req,
                                   cluster_req, split_req, G == 1, variant == POOT_VARIANT_GEMM_TMA);
   const int bm = plan.pair ? 2 * kGemmBM : kGemmBM;
   GemmArgs a;
@@ -554,12 +527,11 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   // within the tile count, hence within int)
   if (a.group_m > a.num_m_blocks) a.group_m = a.num_m_blocks;
   a.num_n_blocks = static_cast<int>((N + plan.bn - 1) / plan.bn);
-  if (plan.cluster == 4) a.num_n_blocks = (a.num_n_blocks + 1) / 2;  // tile pairs along N
   const int64_t num_kb_all = (K + kGemmBK - 1) / kGemmBK;
   const int64_t tiles_per_group = int64_t(a.num_m_blocks) * a.num_n_blocks;
-  // a requested split must divide the K blocks (and is not for groups or
-  // clusters of four); the partial sums need a workspace
-  if (split_req > 1 && (G != 1 || plan.cluster > 2 || num_kb_all % split_req != 0)) return POOT_ERR_INVALID_ARG;
+  // a requested split must divide the K blocks (and is not for groups); the
+  // partial sums need a workspace
+  if (split_req > 1 && (G != 1 || num_kb_all % split_req != 0)) return POOT_ERR_INVALID_ARG;
   int S = plan.split;
   WorkspaceLease lease;
   // workspace: [packed x | packed W | split-K partial sums], 256-byte aligned parts
@@ -659,7 +631,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     const int nkb = a.num_k_blocks, ckb = plan.chunk_kb, tail = nkb % ckb;
     const int shortest = nkb <= ckb ? nkb : (tail == 0 ? ckb : tail);
     const int even_stages = plan.stages & ~1;
-    a.paired = (variant == POOT_VARIANT_GEMM_TMA && plan.cluster <= 2 && ckb % 2 == 0 && nkb % 2 == 0 &&
+    a.paired = (variant == POOT_VARIANT_GEMM_TMA && ckb % 2 == 0 && nkb % 2 == 0 &&
                 even_stages >= 4 && shortest >= even_stages)
                    ? 1
                    : 0;
@@ -676,8 +648,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     const void* xs = packed ? static_cast<const void*>(xp) : x;
     const void* wsrc = packed ? static_cast<const void*>(wp) : w;
     const uint64_t pitch = packed ? static_cast<uint64_t>(Kp) : 0;
-    if (!encode_2d(&tx, xs, K, G * M, kGemmBK, plan.cluster == 4 ? kGemmBM / 2 : kGemmBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B, bf16, pitch) ||
+    if (!encode_2d(&tx, xs, K, G * M, kGemmBK, kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B, bf16, pitch) ||
         !encode_2d(&tw, wsrc, K, G * N, kGemmBK, static_cast<uint32_t>(gemm_b_rows(plan.bn, plan.pair)),
                    CU_TENSOR_MAP_SWIZZLE_128B, bf16, pitch))
       return cuda_fail(cudaErrorInvalidValue);
@@ -716,9 +687,7 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
   }
   if (epi != nullptr || S > 1) {
     // the widened epilogue (and the split-K partial sums) are compiled into
-    // their own instantiations (CTA pairs or single CTAs; clusters of four
-    // are not offered here)
-    if (plan.cluster == 4) return POOT_ERR_INVALID_ARG;
+    // their own instantiations (CTA pairs or single CTAs)
     // head dtype and bias only: the lighter instantiation; FP32 output,
     // steps or split-K partial sums: the full one
     const bool full = S > 1 || a.out_f32 || a.num_steps > 0;
@@ -756,13 +725,6 @@ int launch_gemm(int variant, const DeviceState& st, const void* x, const void* w
     }
     const cudaError_t f = lease.release();
     if (e == cudaSuccess) e = f;
-    return e == cudaSuccess ? POOT_OK : cuda_fail(e);
-  }
-  if (plan.cluster == 4) {
-    const int64_t clusters = st.max_clusters4;
-    const int grid = 4 * static_cast<int>(tiles < clusters ? tiles : clusters);
-    e = launch_clustered(gemm_f16_tcgen05_kernel<kLoadTma, 4>, dim3(grid), dim3(gemm_threads(kLoadTma)),
-                         Layout::DYN_BYTES, stream, 4u, tx, tw, ty, a);
     return e == cudaSuccess ? POOT_OK : cuda_fail(e);
   }
   if (plan.cluster == 2) {
@@ -943,8 +905,7 @@ bool gemm_options_ok(const poot_linear_options& o) {
   if (o.gemm_group_m < 0) return false;
   if (o.gemm_k_chunk < 0 || o.gemm_k_chunk % kGemmBK != 0) return false;
   if (o.gemm_split_k < 0 || o.gemm_split_k > kMaxSplitK) return false;
-  if (o.gemm_split_k > 1 && o.gemm_cluster == 4) return false;
-  return o.gemm_cluster == 0 || o.gemm_cluster == 1 || o.gemm_cluster == 2 || o.gemm_cluster == 4;
+  return o.gemm_cluster == 0 || o.gemm_cluster == 1 || o.gemm_cluster == 2;
 }
 
 int run(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
@@ -1023,7 +984,7 @@ int contract(const void* x, const void* w, const void* b, void* y, int64_t G, in
   std::memset(&o, 0, sizeof(o));
   o.variant = POOT_VARIANT_AUTO;
   if (opts != nullptr) o = *opts;
-  if (!gemm_options_ok(o) || o.gemm_cluster == 4) return POOT_ERR_INVALID_ARG;
+  if (!gemm_options_ok(o)) return POOT_ERR_INVALID_ARG;
   if (o.variant != POOT_VARIANT_AUTO && o.variant != POOT_VARIANT_GEMV && o.variant != POOT_VARIANT_GEMM_TMA &&
       o.variant != POOT_VARIANT_GEMM_CPASYNC && o.variant != POOT_VARIANT_GEMM_REG &&
       o.variant != POOT_VARIANT_GEMM_PACKED)

@@ -140,7 +140,7 @@ def test_bad_gemm_k_chunk(chunk):
         L.POOT_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("cluster", [-1, 3, 8])
+@pytest.mark.parametrize("cluster", [-1, 3, 4, 8])
 def test_bad_gemm_cluster(cluster):
     assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 64, L.options(gemm_cluster=cluster), 0) == \
         L.POOT_ERR_INVALID_ARG
@@ -154,9 +154,7 @@ def test_bad_gemm_split_k(split):
         L.POOT_ERR_INVALID_ARG
 
 
-def test_split_k_refused_with_clusters_of_four_and_groups():
-    assert L.poot_linear_f16_ex(X, W, B, Y, 400, 64, 2048, L.options(gemm_cluster=4, gemm_split_k=2), 0) == \
-        L.POOT_ERR_INVALID_ARG
+def test_split_k_refused_with_groups():
     assert L.poot_contract_grouped(X, W, B, Y, 2, 400, 64, 2048, _spec(), L.options(gemm_split_k=2), 0) == \
         L.POOT_ERR_INVALID_ARG
 

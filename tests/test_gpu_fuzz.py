@@ -108,7 +108,7 @@ def test_random_contraction_exact(case):
 def test_random_linear_normal(case):
     # normal inputs: the 2-ulp rule of the contract, each output beyond it
     # inside the FP32-accumulation interval (tests.parity)
-    from tests.parity import compare, legal_interval
+    from tests.parity import compare, intervals
     rng = np.random.default_rng(9000 + case)
     M, N, K, (ox, ow, oy) = _draw(rng)
     x, w, b = synth.make_inputs(M, N, K, "normal", 9100 + case)
@@ -120,10 +120,11 @@ def test_random_linear_normal(case):
     assert L.poot_linear_device_status(0) == L.POOT_OK
     got = _bits(yd)
     yr, pr = oracle.linear_f16(_bits(x), _bits(w), _bits(b), want_proj=True)
-    interval = legal_interval(x.numpy(), w.numpy(), b.numpy())
+    interval, ieee = intervals(x.numpy(), w.numpy(), b.numpy())
     # every output beyond 2 ulps must lie inside the FP32-accumulation
     # interval; a case of a few ten thousand outputs may hold a handful
     # (the large-workload tests keep the 1e-5 fraction)
-    ok, rep = compare(got, yr, pr, exact=False, interval=interval, max_outside=max(1e-5, 4.0 / got.size))
+    ok, rep = compare(got, yr, pr, exact=False, interval=interval, max_outside=max(1e-5, 4.0 / got.size),
+                      ieee_interval=ieee)
     print(rep)
     assert ok, rep
