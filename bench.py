@@ -8,38 +8,51 @@ A step is one call of poot_linear_f16 on one batch of seeded synthetic
 inputs already resident in HBM.  The default workload is the MLP
 up-projection (M=8192, N=14336, K=4096), the largest configured shape; its
 x + W + y (416 MB) exceed the 129 MB L2, so no flush is needed between
-steps.  Under torchrun (N > 1) every rank runs an independent replica on
-its own GPU (weak scaling, no data-path collective); the step time is the
-maximum over ranks.
+steps.  Exactly K steps are timed (a CUDA graph of the K calls, replayed once
+between two events on the launching stream).  Under torchrun (N > 1) every
+rank runs an independent replica on its own GPU (weak scaling, no data-path
+collective); the step time is the maximum over ranks.
 
 Reported beside the device-timed value:
-  roofline      the GEMM kernel's achieved TFLOP/s (algorithmic 2MNK per
+  roofline      the dominant kernel's achieved TFLOP/s (algorithmic 2MNK per
                 launch / mean CUDA-event duration on its stream) against the
-                measured dense bf16 peak (the fp16 tensor rate is the same);
-                traffic = DRAM bytes per launch from the committed ncu
+                measured dense bf16 burst peak (the fp16 tensor rate is the
+                same); traffic = DRAM bytes per launch from the committed ncu
                 summary when it matches the current kernel source, else null
+  sustained     the same graph replayed back to back for about half a
+                second: time per step, clocks in that window, and the
+                fraction of the measured sustained (power-capped) peak
+  workloads     every other configured shape: graph-timed time per call,
+                its roofline fraction, the kernel that dominates it, and the
+                parity of the device result with the CPU oracle under the
+                contract's rule (full output, or sampled rows on the largest
+                shapes)
   e2e           same metric through the C ABI with host buffers: every step
                 copies its x, W, b host->device (pinned) and its y back,
                 inside the timed region; consecutive steps overlap on three
                 streams (upload / compute / download)
-  cpu_baseline  the CPU oracle timed on a bounded row sample on the host
-                cores (a reported baseline, not the target)
-  clocks        nvidia-smi samples taken during the timed region
+  cpu_baseline  the CPU oracle timed on a bounded row sample on all host
+                cores (a reported baseline, not the target), plus one-core
+                timings of every workload; the sample's rows are compared
+                with the device result under the contract's rule
+  clocks        SM clock and throttle reasons sampled (NVML, every 2 ms)
+                during the timed region
 ``--impl reference`` times the CPU oracle alone on the same workload.
 """
 from __future__ import annotations
 
 import argparse
 import csv
+import ctypes
 import datetime as _dt
 import hashlib
-import io
 import json
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +62,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "TFLOP/s of y=FP16(x·Wᵀ)+b per M×N×K; % of FP16 tensor peak / HBM BW"
 CPU_SAMPLE_SECONDS = 10.0
+WORKLOAD_ORDER = ["toy", "ragged_exact", "gemv_m1", "gemv_m8", "prefill", "mlp_up"]
+# rows of the oracle compared on the shapes too large for a full CPU pass
+PARITY_SAMPLE_ROWS = 256
+# one-core oracle timing: these shapes in full, the others on a row subset
+SINGLE_CORE_FULL = {"toy", "ragged_exact", "gemv_m1", "gemv_m8"}
+SINGLE_CORE_ROWS = 64
+# beyond-2-ulp elements (each inside the FP32-accumulation interval) allowed
+# per element compared, as in the GPU tests
+MAX_BEYOND = 1e-5
 
 
 # Widened-contraction forms for --contract: (head dtype, out_f32, bias, steps);
@@ -74,8 +96,11 @@ def parse_args():
     p.add_argument("--workload", default="mlp_up")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
-    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline and its parity check")
+    p.add_argument("--no-workloads", action="store_true", help="skip the other configured shapes")
     p.add_argument("--cpu-seconds", type=float, default=CPU_SAMPLE_SECONDS)
+    p.add_argument("--sustain-seconds", type=float, default=0.5,
+                   help="length of the back-to-back replay behind the sustained figure (0 = skip)")
     p.add_argument("--variant", default="auto", help="force a kernel variant (auto, gemm_tma, gemv, ...)")
     p.add_argument("--tile-n", type=int, default=0, help="GEMM output tile width (0 = automatic)")
     p.add_argument("--group-m", type=int, default=0, help="GEMM tile-order group (0 = automatic)")
@@ -136,68 +161,149 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (SM clock, reasons) with host timestamps."""
+    """SM clock, power and throttle reasons with host timestamps, sampled in
+    the background: NVML through ctypes every ``period_s`` (reads only), else
+    ``nvidia-smi -lms``.  ``summary(t0, t1)`` describes one window."""
 
-    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_CLOCK_SM = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 20):
-        self.proc = None
-        self.path = None
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.rows = []  # (host time, sm MHz, reason names, power W or None)
+        self.max_mhz = None
+        self.period_s = period_s
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        if self._init_nvml(cuda_index):
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
+            self._thread.start()
+            self.source = f"NVML every {period_s * 1e3:.0f} ms"
+        else:
+            self._init_smi(cuda_index)
+
+    # NVML, read-only queries
+    def _init_nvml(self, cuda_index: int) -> bool:
         try:
-            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 f"-lms={period_ms}"], stdout=self.fh, stderr=subprocess.DEVNULL)
-            deadline = time.time() + 5.0
-            while time.time() < deadline and os.path.getsize(self.path) == 0:
-                time.sleep(0.02)
-        except (OSError, FileNotFoundError):
-            self.proc = None
-
-    def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            ok = False
             try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.fh.close()
+                import torch
+                pr = torch.cuda.get_device_properties(cuda_index)
+                bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except (AttributeError, RuntimeError):
+                ok = False
+            if not ok:
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) == 0
+            if not ok:
+                return False
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            if reasons is None:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(self.NVML_CLOCK_SM), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._nvml, self._h, self._reasons = lib, h, reasons
+            return True
+        except (OSError, AttributeError):
+            return False
 
-    def summary(self, t0: float, t1: float):
-        if self.proc is None or self.path is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _run_nvml(self):
+        lib, h = self._nvml, self._h
+        clk, rs, pw = ctypes.c_uint(0), ctypes.c_ulonglong(0), ctypes.c_uint(0)
+        n = 0
+        while not self._stop.is_set():
+            t = time.time()
+            if lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(self.NVML_CLOCK_SM), ctypes.byref(clk)) == 0:
+                names = []
+                if self._reasons(h, ctypes.byref(rs)) == 0:
+                    names = [v for bit, v in self.REASON_BITS.items() if rs.value & bit]
+                power = None
+                if n % 8 == 0 and lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0:
+                    power = pw.value / 1000.0
+                self.rows.append((t, float(clk.value), names, power))
+            n += 1
+            self._stop.wait(self.period_s)
+
+    # nvidia-smi fallback
+    def _init_smi(self, cuda_index: int):
+        try:
+            fd, self._path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self._fh = open(self._path, "w")
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={cuda_index}", f"--query-gpu={self.SMI_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms=5"], stdout=self._fh, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi -lms 5"
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self._path) == 0:
+                time.sleep(0.02)
+        except OSError:
+            self._proc = None
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         rows = []
-        with open(self.path) as fh:
+        with open(self._path) as fh:
             for r in csv.reader(fh):
                 if len(r) < 10:
                     continue
                 try:
                     ts = _dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(r[2]), float(r[3]), r[4].strip(), [s.strip() for s in r[5:10]]))
+                    act = [names[i] for i in range(4) if r[6 + i].strip().lower() == "active"]
+                    try:
+                        power = float(r[4])
+                    except ValueError:
+                        power = None
+                    rows.append((ts, float(r[2]), act, power))
+                    self.max_mhz = float(r[3])
                 except ValueError:
                     continue
-        os.unlink(self.path)
+        self.rows = rows
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+            self._fh.close()
+            self._read_smi()
+            os.unlink(self._path)
+            self._proc = None
+
+    def summary(self, t0: float, t1: float):
+        if self._proc is not None:
+            self._read_smi()
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples_in_timed_region": 0}
+        rows = list(self.rows)
         inside = [r for r in rows if t0 <= r[0] <= t1]
         used = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
         if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in used for i in range(4) if r[4][i + 1].lower() == "active"})
-        power = []
-        for r in used:
-            try:
-                power.append(float(r[3]))
-            except ValueError:
-                pass
-        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "samples_in_timed_region": 0, "source": self.source}
+        reasons = sorted({n for r in used for n in r[2]})
+        power = [r[3] for r in used if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": self.max_mhz,
                 "sm_min_mhz": min(r[1] for r in used), "reasons": reasons,
                 "power_w_median": statistics.median(power) if power else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(used), "samples_in_timed_region": len(inside)}
+                "samples": len(used), "samples_in_timed_region": len(inside),
+                "window_ms": round((t1 - t0) * 1e3, 3), "source": self.source}
 
 
 def kernel_source_hash() -> str:
@@ -225,17 +331,39 @@ def committed_traffic(kernel: str, workload: str):
     return None
 
 
-# ---- CPU oracle sample ----------------------------------------------------------
-def cpu_oracle_sample(x, w, b, seconds: float, y_gpu=None):
-    """Time the oracle on a row sample sized to about `seconds` of work."""
+def l2_policy(wl):
+    """(copies of x, W, b, y rotated between steps, the statement for `config`)."""
+    working_set = 2 * (wl.M * wl.K + wl.N * wl.K + wl.N + wl.M * wl.N)
+    if working_set >= 3 * L2_BYTES:
+        return 1, "inputs larger than L2 (x+W+b+y = %.0f MB > 129 MB)" % (working_set / 1e6)
+    copies = min(64, -(-3 * L2_BYTES // working_set))
+    return copies, ("inputs larger than L2: %d rotating copies of x, W, b, y (%.0f MB in all)"
+                    % (copies, copies * working_set / 1e6))
+
+
+def workload_config(wl, world):
+    """The `config` object of both arms: what the workload is, nothing measured."""
+    return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "dist": wl.dist, "seed": wl.seed,
+            "accumulate": "f32", "parallelism": "replicas" if world > 1 else "single",
+            "l2": l2_policy(wl)[1]}
+
+
+# ---- CPU oracle -------------------------------------------------------------------
+def _u16(t):
+    import numpy as np
+    import torch
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_oracle_sample(x, w, b, seconds: float):
+    """Time the oracle (all host cores) on a seeded row sample sized to about
+    `seconds` of work; returns (baseline dict, y_ref, p_ref, rows)."""
     import numpy as np
     import oracle
     M, K = x.shape
     N = w.shape[0]
     threads = oracle.default_threads()
-    xb = x.view(torch_int16()).numpy().view(np.uint16)
-    wb = w.view(torch_int16()).numpy().view(np.uint16)
-    bb = b.view(torch_int16()).numpy().view(np.uint16)
+    xb, wb, bb = _u16(x), _u16(w), _u16(b)
     # calibrate on one row per thread
     rows = min(M, threads)
     t = time.perf_counter()
@@ -245,60 +373,192 @@ def cpu_oracle_sample(x, w, b, seconds: float, y_gpu=None):
     want = min(M, want)
     rng = np.random.default_rng(2024)
     sample = np.sort(rng.choice(M, size=want, replace=False))
+    xs = np.ascontiguousarray(xb[sample])
     t = time.perf_counter()
-    y_ref = oracle.linear_f16(np.ascontiguousarray(xb[sample]), wb, bb, nthreads=threads)
+    y_ref, p_ref = oracle.linear_f16(xs, wb, bb, nthreads=threads, want_proj=True)
     dt = time.perf_counter() - t
     flops = 2.0 * want * N * K
     out = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
            "sample": f"{want} of {M} rows (seeded), all {N} columns, K={K}; {dt:.2f} s on {threads} threads",
            "seconds": round(dt, 3)}
-    if y_gpu is not None:
-        g = y_gpu[sample]
-        same = (g == y_ref)
-        out["sample_rows_identical_bits"] = float(same.mean())
-    return out, y_ref, sample
+    return out, y_ref, p_ref, sample
 
 
-def torch_int16():
-    import torch
-    return torch.int16
+def single_core_timings():
+    """The oracle on one core: the small workloads in full, the two largest on
+    a seeded row subset, extrapolated linearly in rows (and labelled so)."""
+    import numpy as np
+    import oracle
+    from linear_fp16_gb300 import synth
+    out = {}
+    for name in WORKLOAD_ORDER:
+        wl = synth.WORKLOADS[name]
+        x, w, b = synth.workload_inputs(name)
+        xb, wb, bb = _u16(x), _u16(w), _u16(b)
+        if name in SINGLE_CORE_FULL:
+            rows = np.arange(wl.M)
+        else:
+            rows = np.sort(np.random.default_rng(77).choice(wl.M, size=SINGLE_CORE_ROWS, replace=False))
+        xs = np.ascontiguousarray(xb[rows])
+        t = time.perf_counter()
+        oracle.linear_f16(xs, wb, bb, nthreads=1)
+        dt = time.perf_counter() - t
+        full_s = dt * wl.M / len(rows)
+        out[name] = {"rows": int(len(rows)), "of_rows": wl.M, "seconds": round(dt, 3),
+                     "seconds_whole_workload": round(full_s, 3),
+                     "extrapolated": len(rows) != wl.M,
+                     "tflops": 2.0 * len(rows) * wl.N * wl.K / dt / 1e12}
+    return out
 
 
-# ---- arms -----------------------------------------------------------------------
-def run_reference(args, rank, world):
+def parity_rows(name, M):
+    """Rows compared with the oracle: all of them, or on the largest shapes a
+    seeded sample that includes the first and last row of every 128-row
+    block boundary it can reach and the ragged last row."""
+    import numpy as np
+    if name in SINGLE_CORE_FULL:
+        return None
+    rng = np.random.default_rng(4040)
+    edges = [0, 127, 128, 255, 256, 383, 384, M - 129, M - 128, M - 1]
+    rest = rng.choice(M, size=PARITY_SAMPLE_ROWS - len(edges), replace=False)
+    return np.unique(np.concatenate([np.array(edges), rest]))
+
+
+def parity_check(name, x, w, b, y_bits, exact, rows=None, y_ref=None, p_ref=None):
+    """The contract's rule on the device result (``oracle.parity``)."""
+    import numpy as np
+    from oracle import parity
+    xb, wb, bb = _u16(x), _u16(w), _u16(b)
+    xs = xb if rows is None else np.ascontiguousarray(xb[rows])
+    yg = y_bits if rows is None else y_bits[rows]
+    if y_ref is None:
+        import oracle
+        y_ref, p_ref = oracle.linear_f16(xs, wb, bb, want_proj=True)
+    ok, rep = parity.judge(yg, y_ref, p_ref, xs, wb, bb, exact, max_outside=MAX_BEYOND)
+    rep = {k: v for k, v in rep.items() if k != "first_bad" or not ok}
+    rep["rule"] = ("bit-exact (small-integer inputs: every FP32 partial sum is exact)" if exact else
+                   "|y - y_ref| <= 2 ulp16(max(|p_ref|, |y_ref|)); beyond that only inside the interval of "
+                   "round-to-nearest FP32 accumulations in any order (u = 2^-24) and at most 1e-5 of the elements")
+    rep["rows"] = "all" if rows is None else f"{len(rows)} of {x.shape[0]} (seeded, block edges included)"
+    rep["ok"] = bool(ok)
+    return rep
+
+
+# ---- the GPU arm -------------------------------------------------------------------
+def kernel_name(L, variant, M):
+    return {L.VARIANT_GEMM_TMA: "gemm_f16_tcgen05_kernel<tma>",
+            L.VARIANT_GEMM_CPASYNC: "gemm_f16_tcgen05_kernel<cpasync4>",
+            L.VARIANT_GEMM_REG: "gemm_f16_tcgen05_kernel<reg16>",
+            L.VARIANT_GEMM_PACKED: "gemm_f16_tcgen05_kernel<tma> (after pack_rows_kernel)",
+            L.VARIANT_GEMV: "gemv_f16_rows_kernel" if M <= 2 else "gemv_f16_mma_kernel",
+            L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
+            }.get(variant, "bias_only_kernel")
+
+
+class Operands:
+    """One workload's x, W, b, y on the device, in as many identical copies as
+    it takes to rotate past L2, and the C-ABI call on copy i % copies."""
+
+    def __init__(self, L, lib, wl, dev, opts):
+        import torch
+        from linear_fp16_gb300 import synth
+        self.L, self.lib, self.wl = L, lib, wl
+        self.x_h, self.w_h, self.b_h = synth.workload_inputs(wl.name)
+        x, w, b = self.x_h.to(dev), self.w_h.to(dev), self.b_h.to(dev)
+        y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+        self.copies, self.l2 = l2_policy(wl)
+        self.sets = [(x, w, b, y)]
+        for _ in range(self.copies - 1):
+            self.sets.append((x.clone(), w.clone(), b.clone(), torch.empty_like(y)))
+        self.ptrs = [tuple(t.data_ptr() for t in s) for s in self.sets]
+        self.opts = opts
+        self.opts_ref = ctypes.byref(opts)
+        self.variant = L.variant_for(x, w, b, y) if opts.variant == L.VARIANT_AUTO else opts.variant
+        self.kernel = kernel_name(L, self.variant, wl.M)
+        self.launches_per_call = 2 if self.variant == L.VARIANT_GEMM_PACKED else 1
+
+    def call(self, i, stream_handle):
+        wl = self.wl
+        rc = self.lib.poot_linear_f16_ex(*self.ptrs[i % self.copies], wl.M, wl.N, wl.K, self.opts_ref,
+                                         stream_handle)
+        if rc != 0:
+            raise RuntimeError(f"poot_linear_f16: {self.L.poot_linear_status_string(rc)}")
+
+    def graph(self, n, first):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream().cuda_stream
+            for i in range(n):
+                self.call(first + i, cap)
+        g.replay()  # one untimed replay: the graph's own first-launch cost
+        torch.cuda.synchronize()
+        return g
+
+    def y_bits(self):
+        return _u16(self.sets[0][3].cpu())
+
+
+def roofline_for(wl, variant, L, seconds_per_call, peaks, src, sustained=False):
+    gemm = variant in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED)
+    if gemm:
+        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
+        achieved = wl.flops / seconds_per_call / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{src} dense bf16 {'sustained' if sustained else 'burst'} "
+                               "(fp16 runs at the bf16 rate)"}
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = wl.algorithmic_bytes / seconds_per_call / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{src} STREAM-style copy"}
+
+
+def measure_workload(L, lib, name, dev, sampler, peaks, src, calls=200, reps=5, check=True):
+    """Graph-timed time per call of one configured shape, its roofline
+    fraction, and the parity of the device result with the oracle."""
     import torch
     from linear_fp16_gb300 import synth
-    if rank != 0:
-        return 0
-    wl = synth.WORKLOADS[args.workload]
-    x, w, b = synth.workload_inputs(args.workload)
-    # each step: a bounded row sample of the workload, sized so that the
-    # whole run stays within a few minutes
-    per_step = max(0.2, min(3.0, 120.0 / (args.steps + args.warmup)))
-    vals = []
-    last = None
-    for i in range(args.warmup + args.steps):
-        res, _, _ = cpu_oracle_sample(x, w, b, per_step)
-        if i >= args.warmup:
-            vals.append(res["value"])
-            last = res
-    value = statistics.mean(vals)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup,
-        # a whole step's time at the sampled rate (each step times a row sample)
-        "ms_per_step": 2.0 * wl.M * wl.N * wl.K / (value * 1e12) * 1e3 if value > 0 else None,
-        "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "dist": wl.dist,
-                   "seed": wl.seed, "accumulate": "f32", "sample": "rows",
-                   "ms_per_step": "extrapolated from the row sample's rate to the whole workload"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
-                         "sample": last["sample"]},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-    return 0
+    wl = synth.WORKLOADS[name]
+    ops = Operands(L, lib, wl, dev, L.options(L.VARIANT_AUTO))
+    stream = torch.cuda.current_stream(dev)
+    for i in range(5):
+        ops.call(i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    if L.poot_linear_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError(f"{name}: device-side wait timed out")
+    g = ops.graph(calls, 5)
+    times = []
+    time.sleep(0.2)  # let the clock settle after the previous measurement
+    w0 = time.time()
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / calls)
+    w1 = time.time()
+    if L.poot_linear_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError(f"{name}: device-side wait timed out")
+    ms = statistics.median(times)
+    roof = roofline_for(wl, ops.variant, L, ms * 1e-3, peaks, src)
+    entry = {"M": wl.M, "N": wl.N, "K": wl.K, "dist": wl.dist, "us_per_call": ms * 1e3,
+             "us_per_call_min": min(times) * 1e3, "us_per_call_each_replay": [round(t * 1e3, 3) for t in times],
+             "calls_per_replay": calls, "replays": reps,
+             "tflops": wl.flops / (ms * 1e-3) / 1e12, "gbs_algorithmic": wl.algorithmic_bytes / (ms * 1e-3) / 1e9,
+             "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_source")},
+             "kernel": ops.kernel, "variant": L.VARIANT_NAMES.get(ops.variant), "launches_per_call":
+                 ops.launches_per_call, "l2": ops.l2, "clocks": sampler.summary(w0, w1) if sampler else None}
+    if ops.launches_per_call > 1:
+        entry["roofline"]["note"] = "time per call covers both launches (operand copy + GEMM)"
+    if check:
+        exact = wl.dist == "smallint"
+        entry["parity"] = parity_check(name, ops.x_h, ops.w_h, ops.b_h, ops.y_bits(), exact,
+                                       rows=parity_rows(name, wl.M))
+    del g, ops
+    torch.cuda.empty_cache()
+    return entry
 
 
 def run_ours(args, rank, world, local):
@@ -313,106 +573,104 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     dist = dist_init(world, True)
     lib = L.load_library()
+    sampler = ClockSampler(local) if rank == 0 else None
 
     wl = synth.WORKLOADS[args.workload]
     M, N, K = wl.M, wl.N, wl.K
-    x_h, w_h, b_h = synth.workload_inputs(args.workload, seed_offset=0)
-    x = x_h.to(dev)
-    w = w_h.to(dev)
-    b = b_h.to(dev)
-    y = torch.empty((M, N), dtype=torch.float16, device=dev)
     variant = L.VARIANT_AUTO
     if args.variant != "auto":
         variant = {v: k for k, v in L.VARIANT_NAMES.items()}[args.variant]
-    chosen = L.variant_for(x, w, b, y) if variant == L.VARIANT_AUTO else variant
+    ops = Operands(L, lib, wl, dev, L.options(variant, 0, args.tile_n, args.group_m, args.k_chunk))
+    chosen = ops.variant
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    # Inputs larger than L2 between steps: when one set of x, W, b, y is
-    # smaller than 3x L2, rotate through enough copies (same values) that a
-    # step never finds its operands in L2 from an earlier step.
-    working_set = 2 * (M * K + N * K + N + M * N)
-    copies = 1
-    if working_set < 3 * L2_BYTES:
-        copies = min(64, -(-3 * L2_BYTES // working_set))
-    sets = [(x, w, b, y)]
-    for _ in range(copies - 1):
-        sets.append((x.clone(), w.clone(), b.clone(), torch.empty_like(y)))
-    ptr_sets = [(a.data_ptr(), bb.data_ptr(), c.data_ptr(), d.data_ptr()) for (a, bb, c, d) in sets]
-    opts = L.options(variant, 0, args.tile_n, args.group_m, args.k_chunk)
-    opts_ref = __import__("ctypes").byref(opts)
-
-    def step(i, stream_handle):
-        rc = lib.poot_linear_f16_ex(*ptr_sets[i % copies], M, N, K, opts_ref, stream_handle)
-        if rc != 0:
-            raise RuntimeError(f"poot_linear_f16: {L.poot_linear_status_string(rc)}")
-
     for i in range(args.warmup):
-        step(i, sh)
+        ops.call(i, sh)
     torch.cuda.synchronize()
     if L.poot_linear_device_status(sh) != 0:
         raise RuntimeError("device-side wait timed out during warm-up")
 
     # The K timed steps are captured once into a CUDA graph and replayed, so
     # a short kernel is not timed together with the host's launch overhead.
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            cap = torch.cuda.current_stream().cuda_stream
-            for i in range(args.steps):
-                step(args.warmup + i, cap)
-        graph.replay()  # one untimed replay: the graph's own first-launch cost
-        torch.cuda.synchronize()
+    graph = None if args.no_graph else ops.graph(args.steps, args.warmup)
 
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 else None
+    def timed_region():
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                ops.call(args.warmup + i, sh)
+        t1.record(stream)
+        return t0, t1
+
+    # ---- burst: exactly K steps ------------------------------------------
     barrier(dist)
     torch.cuda.synchronize()
     wall0 = time.time()
-    t_start.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        for i in range(args.steps):
-            step(args.warmup + i, sh)
-    t_end.record(stream)
+    t_start, t_end = timed_region()
     torch.cuda.synchronize()
     barrier(dist)
     wall1 = time.time()
-    clocks = None
-    if sampler is not None:
-        sampler.stop()
-        clocks = sampler.summary(wall0, wall1)
     total_ms = t_start.elapsed_time(t_end)
     step_ms = max_over_ranks(dist, total_ms / args.steps, dev)
-    # one kernel per step (two for GEMM_PACKED: the row copy, then the
-    # GEMM): the mean duration of the step's kernels is the step time on the
-    # launching stream (graph replay keeps launches back to back)
-    kern_ms = step_ms
-    launches_per_step = 2 if chosen == L.VARIANT_GEMM_PACKED else 1
     if L.poot_linear_device_status(sh) != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
-    y = sets[(args.warmup + args.steps - 1) % copies][3]
+
+    # ---- every other configured shape ---------------------------------------
+    # (measured before the sustained replay, which leaves the GPU at its power
+    # cap for a while; only on rank 0)
+    peaks, src = load_peaks()
+    workloads = None
+    if not args.no_workloads and rank == 0:
+        workloads = {}
+        for name in WORKLOAD_ORDER:
+            if name == wl.name:
+                continue
+            workloads[name] = measure_workload(L, lib, name, dev, sampler, peaks, src, check=not args.no_cpu)
+        torch.cuda.synchronize()
+
+    # ---- sustained: the same K steps back to back for about half a second
+    sustained = None
+    if args.sustain_seconds > 0:
+        reps = max(1, int(args.sustain_seconds / max(total_ms * 1e-3, 1e-6)) + 1)
+        barrier(dist)
+        torch.cuda.synchronize()
+        sw0 = time.time()
+        s0, s1 = timed_region()
+        for _ in range(reps - 1):
+            _, s1 = timed_region()
+        torch.cuda.synchronize()
+        barrier(dist)
+        sw1 = time.time()
+        sus_ms = max_over_ranks(dist, s0.elapsed_time(s1) / (reps * args.steps), dev)
+        sustained = {"ms_per_step": sus_ms, "steps": reps * args.steps, "seconds": round(sw1 - sw0, 3),
+                     "value": world * wl.flops / (sus_ms * 1e-3) / 1e12, "unit": "TFLOP/s"}
+        if sampler is not None:
+            sustained["clocks"] = sampler.summary(sw0, sw1)
+        if L.poot_linear_device_status(sh) != 0:
+            raise RuntimeError("device-side wait timed out during the sustained replay")
 
     # Per-launch distribution, after (and apart from) the timed region: each
     # call launched eagerly between its own pair of events on the launching
-    # stream, rotating the input sets as the timed steps do (so it includes
-    # the host's launch latency that the graph-timed value leaves out).
-    reps = 200 if M <= L.GEMV_MAX_M else 50
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    # stream (so it includes the host's launch latency that the graph-timed
+    # value leaves out).
+    reps_l = 200 if M <= L.GEMV_MAX_M else 50
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps_l)]
     for r, (e0, e1) in enumerate(ev_pairs):
         e0.record(stream)
-        step(args.warmup + args.steps + r, sh)
+        ops.call(args.warmup + args.steps + r, sh)
         e1.record(stream)
     torch.cuda.synchronize()
     per_launch = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev_pairs)
-    per_launch_us = {"reps": reps, "median": per_launch[reps // 2], "p10": per_launch[reps // 10],
-                     "p90": per_launch[(9 * reps) // 10],
+    per_launch_us = {"reps": reps_l, "median": per_launch[reps_l // 2], "p10": per_launch[reps_l // 10],
+                     "p90": per_launch[(9 * reps_l) // 10],
                      "how": "eager launches, each between its own CUDA events (launch latency included)"}
 
-    flops = 2.0 * M * N * K
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    value = world * wl.flops / (step_ms * 1e-3) / 1e12
+    y = ops.sets[0][3]
 
     # ---- end to end through the C ABI with host buffers --------------------
     # Every step uploads its x, W and b from pinned host memory, runs
@@ -421,7 +679,8 @@ def run_ours(args, rank, world, local):
     # streams while step i computes (two device buffer sets).
     e2e = None
     if not args.no_e2e:
-        xp, wp, bp = x_h.pin_memory(), w_h.pin_memory(), b_h.pin_memory()
+        x, w, b = ops.sets[0][:3]
+        xp, wp, bp = ops.x_h.pin_memory(), ops.w_h.pin_memory(), ops.b_h.pin_memory()
         yps = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
         dsets = [(torch.empty_like(x), torch.empty_like(w), torch.empty_like(b), torch.empty_like(y))
                  for _ in range(2)]
@@ -471,10 +730,11 @@ def run_ours(args, rank, world, local):
         e2e_ms = max_over_ranks(dist, a0.elapsed_time(a1) / e2e_steps, dev)
         # the copies made it: the last y on the host equals y on the device
         same = bool(torch.equal(yps[(e2e_steps - 1) % 2], y.cpu()))
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": world * wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(2 * (M * K + N * K + N)), "d2h_bytes_per_step": int(2 * M * N),
                "ms_per_step": e2e_ms, "steps": e2e_steps, "host_y_matches_device_y": same,
                "pipelined": "upload i+1 / compute i / download i-1 on three streams"}
+        del dsets, yps
 
     if rank != 0:
         if dist is not None:
@@ -482,64 +742,96 @@ def run_ours(args, rank, world, local):
         return 0
 
     # ---- roofline of the dominant kernel -----------------------------------
-    peaks, src = load_peaks()
-    gemm = chosen in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED)
-    gemv_vec = "gemv_f16_rows_kernel" if M <= 2 else "gemv_f16_mma_kernel"
-    kernel_name = {L.VARIANT_GEMM_TMA: "gemm_f16_tcgen05_kernel<tma>",
-                   L.VARIANT_GEMM_CPASYNC: "gemm_f16_tcgen05_kernel<cpasync4>",
-                   L.VARIANT_GEMM_REG: "gemm_f16_tcgen05_kernel<reg16>",
-                   L.VARIANT_GEMM_PACKED: "pack_rows_kernel + gemm_f16_tcgen05_kernel<tma>",
-                   L.VARIANT_GEMV: gemv_vec, L.VARIANT_GEMV_SCALAR: "gemv_f16_kernel<scalar>",
-                   }.get(chosen, "bias_only_kernel")
-    kern_s = kern_ms * 1e-3
-    if gemm:
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        achieved = flops / kern_s / 1e12
-        sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_source": f"{src} dense bf16 burst (fp16 runs at the bf16 rate)",
-                "frac_of_sustained_peak": achieved / sustained}
-    else:
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        achieved = wl.algorithmic_bytes / kern_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{src} STREAM-style copy"}
-    roof["traffic"] = committed_traffic(kernel_name, wl.name)
-    roof["kernel"] = kernel_name
-    roof["kernel_ms"] = kern_ms
-    roof["algorithmic_per_launch"] = flops if gemm else wl.algorithmic_bytes
-    roof["hbm_gbs_algorithmic"] = wl.algorithmic_bytes / kern_s / 1e9
+    roof = roofline_for(wl, chosen, L, step_ms * 1e-3, peaks, src)
+    roof["traffic"] = committed_traffic(ops.kernel, wl.name)
+    roof["kernel"] = ops.kernel
+    roof["kernel_ms"] = step_ms
+    roof["algorithmic_per_launch"] = wl.flops if roof["bound"] == "tensor" else wl.algorithmic_bytes
+    roof["hbm_gbs_algorithmic"] = wl.algorithmic_bytes / (step_ms * 1e-3) / 1e9
+    if sustained is not None:
+        sr = roofline_for(wl, chosen, L, sustained["ms_per_step"] * 1e-3, peaks, src, sustained=True)
+        sustained["roofline"] = {k: sr[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_source")}
+
+    y_bits = ops.y_bits()
+    x_h, w_h, b_h = ops.x_h, ops.w_h, ops.b_h
+    del ops, graph
+    torch.cuda.empty_cache()
 
     cpu = None
+    parity = None
     if not args.no_cpu:
-        y_bits = y.cpu().view(torch.int16).numpy().view(np.uint16)
-        cpu, _, _ = cpu_oracle_sample(x_h, w_h, b_h, args.cpu_seconds, y_gpu=y_bits)
+        cpu, y_ref, p_ref, sample = cpu_oracle_sample(x_h, w_h, b_h, args.cpu_seconds)
+        exact = wl.dist == "smallint"
+        parity = parity_check(wl.name, x_h, w_h, b_h, y_bits, exact, rows=sample, y_ref=y_ref, p_ref=p_ref)
+        parity["rows"] = f"the CPU baseline's sample: {len(sample)} of {M} rows (seeded)"
+        cpu["single_core"] = single_core_timings()
+        cpu["single_core_note"] = ("one thread; toy, ragged_exact and both GEMVs in full, prefill and mlp_up on "
+                                   f"{SINGLE_CORE_ROWS} seeded rows with the whole-workload time extrapolated "
+                                   "linearly in rows")
 
+    clocks = sampler.summary(wall0, wall1) if sampler is not None else None
+    if sampler is not None:
+        sampler.stop()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": wl.name, "M": M, "N": N, "K": K, "dist": wl.dist, "seed": wl.seed,
-                   "accumulate": "f32", "variant": L.VARIANT_NAMES.get(chosen, str(chosen)),
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": ("inputs larger than L2 (x+W+b+y = %.0f MB > 129 MB)" % (working_set / 1e6))
-                   if copies == 1 else
-                   "inputs larger than L2: %d rotating copies of x, W, b, y (%.0f MB in all)"
-                   % (copies, copies * working_set / 1e6),
-                   "timing": "CUDA graph of the K steps, replayed between two events" if graph is not None
-                   else "eager launches between two events",
-                   "hbm_gbs_algorithmic": wl.algorithmic_bytes / (step_ms * 1e-3) / 1e9},
+        "config": workload_config(wl, world),
+        "kernel_variant": L.VARIANT_NAMES.get(chosen, str(chosen)),
+        "timing": ("CUDA graph of the K steps, replayed once between two events on the launching stream"
+                   if not args.no_graph else "eager launches between two events"),
         "roofline": roof,
+        "sustained": sustained,
+        "parity": parity,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": args.steps * (2 if chosen == L.VARIANT_GEMM_PACKED else 1),
         "per_launch_us": per_launch_us,
         "clocks": clocks,
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+    return 0
+
+
+# ---- the reference arm: the CPU oracle ----------------------------------------------
+def run_reference(args, rank, world):
+    from linear_fp16_gb300 import synth
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    x, w, b = synth.workload_inputs(args.workload)
+    # each step: a bounded row sample of the workload, sized so that the
+    # whole run stays within a few minutes
+    per_step = max(0.2, min(3.0, 120.0 / (args.steps + args.warmup)))
+    vals, secs = [], []
+    last = None
+    for i in range(args.warmup + args.steps):
+        res, _, _, _ = cpu_oracle_sample(x, w, b, per_step)
+        if i >= args.warmup:
+            vals.append(res["value"])
+            secs.append(res["seconds"])
+            last = res
+    value = statistics.mean(vals)
+    step_ms = statistics.mean(secs) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        # the measured time of a step: one bounded row sample of the workload
+        "ms_per_step": step_ms,
+        "ms_whole_workload_extrapolated": wl.flops / (value * 1e12) * 1e3 if value > 0 else None,
+        "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(wl, world),
+        "timing": "each step: the oracle on a seeded row sample of the workload (all columns, all K), "
+                  "perf_counter around the call",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

@@ -8,8 +8,8 @@ Rules (the readings of the source pages on the widened contraction):
 * otherwise the head value is within the base contract's 2-ulp rule, and y
   must lie within the oracle's epilogue applied to its head value +-2 ulps
   (the hull), widened by 2 ulps for those exp / erf roundings;
-* FP32 output: the sum error bound gamma_K sum|x w| with u = 2^-23 (an
-  accumulator that truncates), plus one FP32 rounding of the bias add.
+* FP32 output: the sum error bound gamma_K sum|x w| with u = 2^-24 (any
+  round-to-nearest FP32 order), plus one FP32 rounding of the bias add.
 """
 import numpy as np
 import pytest
@@ -114,7 +114,7 @@ def _check_head(x, w, b, steps, y, dt, exact_sums, rows=None):
     inside = same | ((gv >= lo - 2 * _ulp(lo, dt)) & (gv <= hi + 2 * _ulp(hi, dt)))
     # outside the hull: a cancelling sum whose head value moved more than 2
     # ulps; legal if y is the epilogue of some head value that an FP32 sum of
-    # the same products can round to (Higham's bound, u = 2^-23)
+    # the same products can round to (Higham's bound, u = 2^-24)
     outl = np.argwhere(~inside)
     for m, n in outl:
         assert _in_interval_image(xs, w, b, st, m, n, gv[m, n], dt), \
@@ -129,7 +129,7 @@ def _in_interval_image(xs, w, b, st, m, n, yv, dt):
     S = float((xv * wv).sum())
     A = float((xv * wv).abs().sum())
     K = xv.numel()
-    u = 2.0 ** -23
+    u = 2.0 ** -24
     E = K * u / (1 - K * u) * A
     conv = oracle.f64_to_f16_rn if dt == "f16" else oracle.f64_to_bf16_rn
     k_lo, k_hi = (_key(conv([S - E])[0]), _key(conv([S + E])[0]))
@@ -158,12 +158,14 @@ def _check_f32(x, w, b, y, dt, exact_sums):
     S = (xs @ ws.T).numpy()
     A = (xs.abs() @ ws.abs().T).numpy()
     K = x.shape[1]
-    u = 2.0 ** -23
+    u = 2.0 ** -24
     bound = K * u / (1 - K * u) * A
     if b is not None:
         S = S + b.double().numpy() if dt == "f16" else S + b.float().double().numpy()
         bound = bound + np.abs(S) * 2.0 ** -24
-    assert np.all(np.abs(yg - S) <= bound + 1e-30)
+    err = np.abs(yg - S)
+    print(f"FP32 output: largest error / bound {float((err / (bound + 1e-30)).max()):.4f}")
+    assert np.all(err <= bound + 1e-30)
 
 
 # ---- head dtype, bias, no steps ---------------------------------------------------

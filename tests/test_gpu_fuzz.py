@@ -120,11 +120,11 @@ def test_random_linear_normal(case):
     assert L.poot_linear_device_status(0) == L.POOT_OK
     got = _bits(yd)
     yr, pr = oracle.linear_f16(_bits(x), _bits(w), _bits(b), want_proj=True)
-    interval, ieee = intervals(x.numpy(), w.numpy(), b.numpy())
+    interval, wide = intervals(x.numpy(), w.numpy(), b.numpy())
     # every output beyond 2 ulps must lie inside the FP32-accumulation
     # interval; a case of a few ten thousand outputs may hold a handful
     # (the large-workload tests keep the 1e-5 fraction)
     ok, rep = compare(got, yr, pr, exact=False, interval=interval, max_outside=max(1e-5, 4.0 / got.size),
-                      ieee_interval=ieee)
+                      wide_interval=wide)
     print(rep)
     assert ok, rep

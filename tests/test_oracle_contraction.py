@@ -13,6 +13,7 @@ pages and the mathematics fix, without a GPU.
   bfloat16 head (sums exact, so only the stated roundings remain).
 """
 import math
+import os
 from fractions import Fraction
 
 import numpy as np
@@ -91,7 +92,22 @@ def test_bf16_decode_is_the_upper_half_of_binary32():
 
 # ---- epilogue chains --------------------------------------------------------------
 @pytest.mark.parametrize("name", ["epilogue_silu.txt", "epilogue_gelu.txt"])
-def test_hand_worked_chains(name):
+def test_stored_chains_are_what_the_derivation_script_writes(name):
+    # the fixtures' values come from tests/golden/derive_epilogue_chains.py,
+    # which imports neither the oracle nor the CUDA package
+    import importlib.util
+    path = os.path.join(os.path.dirname(__file__), "golden", "derive_epilogue_chains.py")
+    spec = importlib.util.spec_from_file_location("derive_epilogue_chains", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    _, cases = mod.derive(name)
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as fh:
+        stored = [ln.strip() for ln in fh if ln.startswith("case ")]
+    assert cases == stored
+
+
+@pytest.mark.parametrize("name", ["epilogue_silu.txt", "epilogue_gelu.txt"])
+def test_worked_chains(name):
     for dtype, op, t, y in exact.parse_chain_golden(name):
         got = _chain([t], op, dtype)[0]
         assert got == y, (dtype, op, t, got, y)

@@ -81,15 +81,17 @@ def test_ieee_interval_holds_round_to_nearest_orders():
     # sequential sum and a pairwise one both lie inside it, and it nests in
     # the wider interval that also admits truncation
     x, w, b = synth.make_inputs(48, 80, 2000, "normal", 6)
-    (lo_t, hi_t), (lo, hi) = intervals(x.numpy(), w.numpy(), b.numpy())
+    (lo, hi), (lo_t, hi_t) = intervals(x.numpy(), w.numpy(), b.numpy())
     assert np.all(lo_t <= lo) and np.all(hi <= hi_t)
+    assert np.array_equal(np.stack(legal_interval(x.numpy(), w.numpy(), b.numpy())), np.stack((lo, hi)))
     assert np.array_equal(np.stack(legal_interval(x.numpy(), w.numpy(), b.numpy(), u=U_RN)), np.stack((lo, hi)))
     yr, pr = oracle.linear_f16(_bits(x), _bits(w), _bits(b), want_proj=True)
     for y in (yr.view(np.float16), _other_order(x, w, b)):
         v = y.astype(np.float64)
         assert np.all((v >= lo) & (v <= hi))
-        ok, rep = compare(y.view(np.uint16), yr, pr, exact=False, interval=(lo_t, hi_t), ieee_interval=(lo, hi))
-        assert ok and rep["beyond_2ulp_outside_ieee_interval"] == 0, rep
+        ok, rep = compare(y.view(np.uint16), yr, pr, exact=False, interval=(lo, hi), wide_interval=(lo_t, hi_t))
+        assert ok and rep["beyond_2ulp_outside_interval"] == 0, rep
+        assert rep["beyond_2ulp_outside_truncating_interval"] == 0, rep
 
 
 def test_check_rows_matches_compare_and_counts_strict_ulps():
@@ -102,7 +104,7 @@ def test_check_rows_matches_compare_and_counts_strict_ulps():
     bad = yr[rows].copy()
     bad[1, 5] = np.uint16(int(bad[1, 5]) + 3) if (bad[1, 5] & 0x7c00) != 0x7c00 else bad[1, 5]
     ok, rep = check_rows(bad, _bits(x), _bits(w), _bits(b), exact=False, rows=rows)
-    assert not ok and rep["beyond_2ulp_of_y"] == 1 and rep["beyond_2ulp_outside_ieee_interval"] == 1
+    assert not ok and rep["beyond_2ulp_of_y"] == 1 and rep["beyond_2ulp_outside_interval"] == 1
     # the dropped-term mutation fails through check_rows too
     dropped = oracle.linear_f16(_bits(x), _bits(w), _bits(b), mutation=3)
     ok, rep = check_rows(dropped, _bits(x), _bits(w), _bits(b), exact=False)

@@ -2,10 +2,12 @@
 library's fixed device array.
 
 Its results must be the bits poot_linear_f16_ex gives with the same GEMM
-variant and split factor.  Two calls in a row (the second reusing the array
-the first wrote) are each compared with that entry point; argument and size
-errors are checked before any CUDA call.  The file name keeps it last in
-collection; it also passes on its own.
+variant and split factor, and must match the CPU oracle under the
+contract's rule (bit-exact on small integers, else the 2-ulp rule with the
+FP32-accumulation interval).  Two calls in a row (the second reusing the
+array the first wrote) are each compared with that entry point and with the
+oracle; argument and size errors are checked before any CUDA call.  The
+file name keeps it last in collection; it also passes on its own.
 """
 import re
 from pathlib import Path
@@ -16,6 +18,7 @@ import torch
 
 import linear_fp16_gb300 as L
 from linear_fp16_gb300 import synth
+from tests.parity import check_rows
 
 ROOT = Path(__file__).resolve().parents[1]
 X, W, B, Y = 0x1000_0000_0, 0x2000_0000_0, 0x3000_0000_0, 0x4000_0000_0   # never dereferenced
@@ -69,13 +72,17 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
     cases = [((128, 1024, 4096), 4, "normal", 11), ((64, 2048, 8192), 8, "smallint", 12)]
     outs = []
     for (M, N, K), S, dist, seed in cases:
-        x, w, b = (t.to(DEV) for t in synth.make_inputs(M, N, K, dist, seed))
-        outs.append(_run_both(x, w, b, S, L.VARIANT_GEMM_TMA))
+        xh, wh, bh = synth.make_inputs(M, N, K, dist, seed)
+        x, w, b = xh.to(DEV), wh.to(DEV), bh.to(DEV)
+        outs.append((_run_both(x, w, b, S, L.VARIANT_GEMM_TMA), (xh, wh, bh), dist == "smallint"))
     torch.cuda.synchronize()
     assert L.poot_linear_device_status(0) == L.POOT_OK
-    for y_na, y_ex in outs:
+    for (y_na, y_ex), (xh, wh, bh), exact in outs:
         assert not torch.isnan(y_na).any()
         assert np.array_equal(_bits(y_na), _bits(y_ex))
+        u16 = lambda t: _bits(t).view(np.uint16)
+        ok, rep = check_rows(u16(y_na), u16(xh), u16(wh), u16(bh), exact=exact)
+        assert ok, rep
 
 
 @pytest.mark.gpu
