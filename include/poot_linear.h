@@ -327,6 +327,63 @@ POOT_API int poot_contract_grouped(const void* x, const void* w, const void* b, 
 POOT_API int poot_linear_f16_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M,
                                             int64_t N, int64_t K, int split_k, poot_stream_t stream);
 
+/* ---- Tensor-parallel linear -----------------------------------------------
+ *
+ * "The Graph IR", Primitive operations, the AllReduce / AllGather row
+ * (tensor-parallel collectives; AllGather multiplies the gather axis by the
+ * number of ranks), and "Model and Distributed IR", section "Boundary between
+ * the layers" (linear(x, w) with a tensor-parallel strategy becomes
+ * rank-local matmul tasks, a collective, and a reconstructed result that
+ * equals the source semantics).  The collective itself is the caller's (NCCL
+ * through torch.distributed in the Python binding); these are the host plan
+ * and the device steps around it:
+ *
+ *   column split (over N): rank r holds W[begin_r:end_r, :] and b[begin_r:end_r]
+ *     and computes y_r = poot_linear_f16(x, W_r, b_r) ([M, N_r], bit-identical
+ *     to those columns of the one-GPU result); an all-gather puts every y_r
+ *     in its slot; poot_linear_gather_columns assembles y [M, N].
+ *   row split (over K): rank r holds x[:, begin_r:end_r] and
+ *     W[:, begin_r:end_r] and computes the FP32 partial sums S_r with
+ *     poot_contract (out_f32, no bias); an all-reduce adds them in FP32 (one
+ *     legal summation order, rule 1 of the contract); poot_linear_f16_finish
+ *     rounds once: y = RN16(RN16(S) + b).  Rounding or adding b per rank
+ *     before the reduction would break the contract's rule 2.
+ */
+
+/*
+ * Shard [*begin, *end) of rank `rank` among `world` ranks over an axis of
+ * `extent` elements: contiguous ranges, every one but the last
+ * ceil(extent / world) rounded up to a multiple of 8 wide (so a shard of a
+ * 16-byte-aligned row-major operand stays 16-byte aligned), trailing ranks
+ * possibly empty.  Pure host logic, no CUDA call.
+ * Errors: POOT_ERR_INVALID_ARG for extent outside [0, 2^31), world outside
+ * [1, 65536], rank outside [0, world), or a NULL output pointer.
+ */
+POOT_API int poot_linear_tp_shard(int64_t extent, int world, int rank, int64_t* begin, int64_t* end);
+
+/*
+ * y [M, N] (row-major binary16, device) from the column shards of a
+ * tensor-parallel linear: slots (device) holds `world` slots of slot_elems
+ * elements each, slot r holding rank r's y_r [M, N_r] row-major, its
+ * columns [begin_r, end_r) as poot_linear_tp_shard(N, world, r) gives them.
+ * A pure copy (bits unchanged), on `stream`, asynchronous.
+ * slot_elems must hold the widest shard (M * N_0); y must not overlap the
+ * slots.  Errors: POOT_ERR_INVALID_ARG (sizes, NULL, overlap),
+ * POOT_ERR_MISALIGNED (a pointer not 2-byte aligned), POOT_ERR_CUDA.
+ */
+POOT_API int poot_linear_gather_columns(const void* slots, void* y, int64_t M, int64_t N, int world,
+                                        int64_t slot_elems, poot_stream_t stream);
+
+/*
+ * y = RN16(RN16(S) + b) for an FP32 sum S [M, N] (device, row-major; the
+ * all-reduced partial sums of a row split), b [N] and y [M, N] binary16
+ * (device).  The epilogue of poot_linear_f16 applied to a given sum, on
+ * `stream`, asynchronous.  S 4-byte aligned, b and y 2-byte aligned, y not
+ * overlapping S or b.  Errors as poot_linear_gather_columns.
+ */
+POOT_API int poot_linear_f16_finish(const float* S, const void* b, void* y, int64_t M, int64_t N,
+                                    poot_stream_t stream);
+
 /* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
 POOT_API int poot_linear_version(void);
 

@@ -2,6 +2,8 @@
 
 ``linear(x, w, b)`` is the tensor-level call, and ``contract`` the widened
 contraction (bfloat16 heads, no bias, FP32 output, fused epilogue steps);
+``column_parallel_linear`` and ``row_parallel_linear`` split the op over
+torch.distributed ranks;
 the C entry points of include/poot_linear.h are mirrored one to one in
 ``binding``.
 """
@@ -16,6 +18,10 @@ from .binding import (  # noqa: F401
     ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,
     EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract, poot_contract_grouped,
     NOALLOC_SCRATCH_BYTES, poot_linear_f16_splitk_noalloc,
+    poot_linear_tp_shard, poot_linear_gather_columns, poot_linear_f16_finish,
+)
+from .tensor_parallel import (  # noqa: F401
+    shard_range, column_parallel_linear, row_parallel_linear,
 )
 
 __version__ = "0.1.0"

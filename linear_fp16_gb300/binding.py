@@ -95,6 +95,10 @@ EXPORTS = {
     "poot_contract_grouped": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64,
                                              ctypes.POINTER(ContractionSpec), ctypes.POINTER(Options), _VP]),
     "poot_linear_f16_splitk_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP]),
+    "poot_linear_tp_shard": (ctypes.c_int, [_I64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_I64),
+                                            ctypes.POINTER(_I64)]),
+    "poot_linear_gather_columns": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_int, _I64, _VP]),
+    "poot_linear_f16_finish": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, _VP]),
 }
 
 _lock = threading.Lock()
@@ -149,6 +153,24 @@ def poot_linear_f16_splitk_noalloc(x: int, w: int, b: int, y: int, M: int, N: in
                                    stream: int) -> int:
     """Split-K with its partial sums in the library's fixed device array (no allocation)."""
     return load_library().poot_linear_f16_splitk_noalloc(x, w, b, y, M, N, K, split_k, stream)
+
+
+def poot_linear_tp_shard(extent: int, world: int, rank: int):
+    """(status, begin, end) of rank's shard of an axis of `extent` elements (host only)."""
+    b, e = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = load_library().poot_linear_tp_shard(extent, world, rank, ctypes.byref(b), ctypes.byref(e))
+    return rc, b.value, e.value
+
+
+def poot_linear_gather_columns(slots: int, y: int, M: int, N: int, world: int, slot_elems: int,
+                               stream: int) -> int:
+    """y [M,N] from the column shards in `world` slots of slot_elems elements."""
+    return load_library().poot_linear_gather_columns(slots, y, M, N, world, slot_elems, stream)
+
+
+def poot_linear_f16_finish(S: int, b: int, y: int, M: int, N: int, stream: int) -> int:
+    """y = RN16(RN16(S) + b) for an FP32 sum S [M,N]."""
+    return load_library().poot_linear_f16_finish(S, b, y, M, N, stream)
 
 
 def poot_linear_f16_variant(x: int, w: int, b: int, y: int, M: int, N: int, K: int) -> int:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpoot_linear.so")
 SOURCES = [os.path.join(CSRC, "poot_linear.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "gemm_tcgen05.cuh", "gemv.cuh", "epilogue.cuh", "splitk.cuh", "pack.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "gemm_tcgen05.cuh", "gemv.cuh", "epilogue.cuh", "splitk.cuh", "pack.cuh", "shards.cuh")] + [
     os.path.join(INCLUDE, "poot_linear.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -340,6 +340,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     tma_prefetch_desc(&tm_w);
   }
   if (warp == 0 && lane == 0 && args.tma_store) tma_prefetch_desc(&tm_y);
+  // the next kernel in the stream may start launching now: its CTAs can only
+  // take SMs this grid leaves free, and it touches global memory only after
+  // this grid has completed (its own grid_dep_wait)
+  grid_dep_launch();
   tc_fence_before_sync();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote signal
@@ -347,7 +351,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   const uint32_t tmem_base = *tmem_slot;
   // prologue done; global memory is touched only after the previous grid
   grid_dep_wait();
-  grid_dep_launch();
 
   if (warp >= kGemmProdWarp0) {
     // ------------------------------------------------------------ producer
@@ -383,8 +386,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               if (!mbar_wait(bar_cfull(pc & 1), (uint32_t)((pc >> 1) & 1), abort_flag)) { ok = false; break; }
               mbar_arrive(eb);  // in place of the MMA's commit
             }
-            if (!mbar_wait(eb, phase ^ 1u, abort_flag)) { ok = false; break; }
-            if (paired && leader && ck == 0) {
+            // the first pass over the ring and the first two chunk buffers
+            // find them free: no wait (it would only add latency to the start)
+            if (issued >= STAGES && !mbar_wait(eb, phase ^ 1u, abort_flag)) { ok = false; break; }
+            if (paired && leader && ck == 0 && ch >= 2) {
               // the chunk's TMEM buffer must be drained before its first MMA;
               // that MMA waits on this stage's full barrier, so the producer
               // waits for the buffer before arming the barrier
@@ -633,16 +638,18 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       }
       if (!ok) break;
       // final epilogue of this tile from registers; lane l of box g holds
-      // b[n0 + col0 + 32g + l], all boxes loaded together
+      // b[n0 + col0 + 32g + l], all boxes loaded together (the plain
+      // epilogue reads whole aligned boxes as broadcast vectors instead)
       // this tile's group: its bias and output (step operands below)
       const __half* bg = args.b + (size_t)grp * N;
       __half* yg = args.y + (size_t)grp * M * N;
       unsigned short bias16[kGemmHalfCols / 32];
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
-        const int col = n0 + col0 + g * 32 + lane;
-        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(bg[col])
-                                                                         : (unsigned short)0;
+        const int nc = n0 + col0 + g * 32, col = nc + lane;
+        const bool bvec = !GEN && nc + 32 <= N && (reinterpret_cast<uintptr_t>(bg + nc) & 15u) == 0;
+        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N && !bvec) ? __half_as_ushort(bg[col])
+                                                                                  : (unsigned short)0;
       }
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
@@ -712,13 +719,27 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           }
           uint32_t packed[16];
           if constexpr (!GEN) {
+            // b[nc .. nc+31] as 16 column pairs: four 16-byte loads of the
+            // same address by every lane (one broadcast request each) when
+            // the box is whole and aligned, else by shuffles of bias16
+            uint32_t bw[16];
+            if (nc + 32 <= N && (reinterpret_cast<uintptr_t>(bg + nc) & 15u) == 0) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(bg + nc) + j);
+                bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                bw[i] = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
+                        ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               // proj = RN16(acc) for two columns, then y = RN16(proj + b)
               const __half2 p = __floats2half2_rn(acc[g * 32 + 2 * i], acc[g * 32 + 2 * i + 1]);
-              const uint32_t b2 = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
-                                  ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
-              const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&b2));
+              const __half2 yv = __hadd2(p, *reinterpret_cast<const __half2*>(&bw[i]));
               packed[i] = *reinterpret_cast<const uint32_t*>(&yv);
             }
           } else {
@@ -800,7 +821,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         }
       }
     }
-    if (args.tma_store && lane == 0) bulk_wait_group<0>();
+    // the staging buffers must have been read before the CTA exits; the
+    // stores' writes complete with the grid (a dependent kernel's
+    // grid_dep_wait sees them)
+    if (args.tma_store && lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 

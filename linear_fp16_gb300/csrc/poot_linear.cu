@@ -18,6 +18,7 @@
 #include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
 #include "pack.cuh"
+#include "shards.cuh"
 #include "splitk.cuh"
 
 namespace {
@@ -1082,6 +1083,91 @@ int run_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int
                      POOT_NOALLOC_SCRATCH_BYTES);
 }
 
+// ---- tensor-parallel helpers -------------------------------------------------
+// Shard plan of a tensor-parallel linear over `world` ranks: contiguous ranges
+// of `extent` (N for a column split, K for a row split), every range but the
+// last `width` elements wide, width a multiple of 8 so that every shard of a
+// 16-byte-aligned operand stays 16-byte aligned (its TMA path applies).
+int64_t tp_width(int64_t extent, int world) {
+  int64_t w = (extent + world - 1) / world;
+  w = (w + 7) / 8 * 8;
+  return w < 8 ? 8 : w;
+}
+
+void tp_shard(int64_t extent, int world, int rank, int64_t* begin, int64_t* end) {
+  const int64_t w = tp_width(extent, world);
+  const int64_t b = int64_t(rank) * w, e = b + w;
+  *begin = b < extent ? b : extent;
+  *end = e < extent ? e : extent;
+}
+
+int gather_columns(const void* slots, void* y, int64_t M, int64_t N, int world, int64_t slot_elems,
+                   cudaStream_t stream) {
+  if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim || world < 1 || world > 65536 || slot_elems < 0)
+    return POOT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return POOT_OK;
+  if (slots == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
+  if (!aligned(slots, 2) || !aligned(y, 2)) return POOT_ERR_MISALIGNED;
+  const int64_t width = tp_width(N, world);
+  // the first shard is the widest; every slot must hold it, and the shards
+  // must cover N
+  const int64_t w0 = width < N ? width : N;
+  if (slot_elems < M * w0 || width * int64_t(world) < N) return POOT_ERR_INVALID_ARG;
+  if (overlaps(y, M * N * 2, slots, int64_t(world) * slot_elems * 2)) return POOT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  const int rc = device_state(&dev, &st);
+  if (rc != POOT_OK) return rc;
+  GatherColumnsArgs a;
+  a.slots = static_cast<const uint16_t*>(slots);
+  a.y = static_cast<uint16_t*>(y);
+  a.M = M;
+  a.N = N;
+  a.slot_elems = slot_elems;
+  a.width = width;
+  a.world = world;
+  const int64_t chunks = M * ((N + 7) / 8);
+  int64_t blocks = (chunks + 255) / 256;
+  const int64_t cap = int64_t(st->sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  const cudaError_t e = launch(gather_columns_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
+  return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+}
+
+int finish_f16(const float* S, const void* b, void* y, int64_t M, int64_t N, cudaStream_t stream) {
+  if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim) return POOT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return POOT_OK;
+  if (S == nullptr || b == nullptr || y == nullptr) return POOT_ERR_INVALID_ARG;
+  if (!aligned(S, 4) || !aligned(b, 2) || !aligned(y, 2)) return POOT_ERR_MISALIGNED;
+  if (overlaps(y, M * N * 2, S, M * N * 4) || overlaps(y, M * N * 2, b, N * 2)) return POOT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  const int rc = device_state(&dev, &st);
+  if (rc != POOT_OK) return rc;
+  // the split-K reduce with one partial: y = RN16(RN16(S) + b)
+  SplitReduceArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.ws = S;
+  ra.S = 1;
+  ra.M = static_cast<int>(M);
+  ra.N = static_cast<int>(N);
+  ra.e.dtype = POOT_DTYPE_F16;
+  ra.e.has_bias = 1;
+  ra.e.b = static_cast<const uint16_t*>(b);
+  ra.e.y = static_cast<uint16_t*>(y);
+  ra.e.ldy = N;
+  const bool vec = N % 4 == 0 && aligned(S, 16) && aligned(y, 8);
+  const int64_t units = vec ? M * N / 4 : M * N;
+  int64_t blocks = (units + 255) / 256;
+  const int64_t cap = int64_t(st->sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  const cudaError_t e = vec ? launch(splitk_reduce_kernel<4>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     stream, ra)
+                            : launch(splitk_reduce_kernel<1>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     stream, ra);
+  return e == cudaSuccess ? POOT_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1100,6 +1186,23 @@ int poot_contract_grouped(const void* x, const void* w, const void* b, void* y, 
 int poot_linear_f16_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N,
                                    int64_t K, int split_k, poot_stream_t stream) {
   return run_splitk_noalloc(x, w, b, y, M, N, K, split_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_tp_shard(int64_t extent, int world, int rank, int64_t* begin, int64_t* end) {
+  if (extent < 0 || extent > kMaxDim || world < 1 || world > 65536 || rank < 0 || rank >= world ||
+      begin == nullptr || end == nullptr)
+    return POOT_ERR_INVALID_ARG;
+  tp_shard(extent, world, rank, begin, end);
+  return POOT_OK;
+}
+
+int poot_linear_gather_columns(const void* slots, void* y, int64_t M, int64_t N, int world, int64_t slot_elems,
+                               poot_stream_t stream) {
+  return gather_columns(slots, y, M, N, world, slot_elems, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_f16_finish(const float* S, const void* b, void* y, int64_t M, int64_t N, poot_stream_t stream) {
+  return finish_f16(S, b, y, M, N, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int poot_linear_f16(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N, int64_t K,
