@@ -499,6 +499,14 @@ class Operands:
         return _u16(self.sets[0][3].cpu())
 
 
+def gemm_plan(L, wl):
+    """The GEMM's automatic tile plan for this shape on this device (host logic)."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rc, plan = L.poot_linear_gemm_plan(wl.M, wl.N, wl.K, sms)
+    return plan if rc == 0 else None
+
+
 def roofline_for(wl, variant, L, seconds_per_call, peaks, src, sustained=False):
     gemm = variant in (L.VARIANT_GEMM_TMA, L.VARIANT_GEMM_CPASYNC, L.VARIANT_GEMM_REG, L.VARIANT_GEMM_PACKED)
     if gemm:
@@ -552,6 +560,7 @@ def measure_workload(L, lib, name, dev, sampler, peaks, src, calls=200, reps=5, 
                  ops.launches_per_call, "l2": ops.l2, "clocks": sampler.summary(w0, w1) if sampler else None}
     if ops.launches_per_call > 1:
         entry["roofline"]["note"] = "time per call covers both launches (operand copy + GEMM)"
+    entry["gemm_plan"] = gemm_plan(L, wl) if wl.M > L.GEMV_MAX_M else None
     if check:
         exact = wl.dist == "smallint"
         entry["parity"] = parity_check(name, ops.x_h, ops.w_h, ops.b_h, ops.y_bits(), exact,
@@ -748,6 +757,7 @@ def run_ours(args, rank, world, local):
     roof["kernel_ms"] = step_ms
     roof["algorithmic_per_launch"] = wl.flops if roof["bound"] == "tensor" else wl.algorithmic_bytes
     roof["hbm_gbs_algorithmic"] = wl.algorithmic_bytes / (step_ms * 1e-3) / 1e9
+    roof["gemm_plan"] = gemm_plan(L, wl) if M > L.GEMV_MAX_M else None
     if sustained is not None:
         sr = roofline_for(wl, chosen, L, sustained["ms_per_step"] * 1e-3, peaks, src, sustained=True)
         sustained["roofline"] = {k: sr[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_source")}

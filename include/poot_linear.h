@@ -187,7 +187,24 @@ POOT_API int poot_linear_f16_ex(const void* x, const void* w, const void* b, voi
 POOT_API int poot_linear_f16_variant(const void* x, const void* w, const void* b, const void* y,
                             int64_t M, int64_t N, int64_t K);
 
-/* Static, NUL-terminated description of a status code (never NULL). */
+/*
+ * The GEMM's tile plan for y = FP16(x . W^T) + b with x and W readable by
+ * TMA in place and every option automatic, on a device with `sm_count` SMs
+ * (pure host logic, no CUDA call: tests and benchmarks use it to see which
+ * plan runs).  Errors: POOT_ERR_INVALID_ARG for sizes outside [1, 2^31),
+ * sm_count < 2 or a NULL out.
+ */
+typedef struct poot_gemm_plan {
+    int tile_n;     /* output tile width (the MMA's N) */
+    int cluster;    /* 1: single CTAs, 128-row tiles; 2: CTA pairs, 256-row tiles */
+    int split_k;    /* K ranges summed by separate tiles (1: none) */
+    int k_chunk;    /* K elements per TMEM accumulation chain */
+    int tiles;      /* output tiles (times split_k) */
+    int ctas;       /* CTAs of a full grid (persistent: at most one per SM) */
+} poot_gemm_plan;
+POOT_API int poot_linear_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, poot_gemm_plan* out);
+
+/* Static, NUL-terminated description of a status code (never NULL). *//* Static, NUL-terminated description of a status code (never NULL). */
 POOT_API const char* poot_linear_status_string(int status);
 
 /* Name of the CUDA error behind the calling thread's last POOT_ERR_CUDA

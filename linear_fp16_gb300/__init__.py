@@ -18,7 +18,7 @@ from .binding import (  # noqa: F401
     ContractionSpec, DTYPE_BF16, DTYPE_F16, EP_ADD, EP_GELU_ERF, EP_GELU_TANH, EP_MUL, EP_SILU,
     EPILOGUE_MAX_STEPS, EpilogueStep, contract, poot_contract, poot_contract_grouped,
     NOALLOC_SCRATCH_BYTES, poot_linear_f16_splitk_noalloc,
-    poot_linear_tp_shard, poot_linear_gather_columns, poot_linear_f16_finish,
+    poot_linear_tp_shard, poot_linear_gather_columns, poot_linear_f16_finish, poot_linear_gemm_plan,
 )
 from .tensor_parallel import (  # noqa: F401
     shard_range, column_parallel_linear, row_parallel_linear,

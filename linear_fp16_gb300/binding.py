@@ -67,6 +67,11 @@ def options(variant: int = -1, gemv_warps_per_row: int = 0, gemm_tile_n: int = 0
                    gemm_split_k)
 
 
+class GemmPlan(ctypes.Structure):
+    """struct poot_gemm_plan."""
+    _fields_ = [(n, ctypes.c_int) for n in ("tile_n", "cluster", "split_k", "k_chunk", "tiles", "ctas")]
+
+
 class EpilogueStep(ctypes.Structure):
     """struct poot_epilogue_step."""
     _fields_ = [("op", ctypes.c_int), ("operand", ctypes.c_void_p), ("ld", ctypes.c_int64)]
@@ -95,6 +100,7 @@ EXPORTS = {
     "poot_contract_grouped": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64,
                                              ctypes.POINTER(ContractionSpec), ctypes.POINTER(Options), _VP]),
     "poot_linear_f16_splitk_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP]),
+    "poot_linear_gemm_plan": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(GemmPlan)]),
     "poot_linear_tp_shard": (ctypes.c_int, [_I64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_I64),
                                             ctypes.POINTER(_I64)]),
     "poot_linear_gather_columns": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_int, _I64, _VP]),
@@ -153,6 +159,13 @@ def poot_linear_f16_splitk_noalloc(x: int, w: int, b: int, y: int, M: int, N: in
                                    stream: int) -> int:
     """Split-K with its partial sums in the library's fixed device array (no allocation)."""
     return load_library().poot_linear_f16_splitk_noalloc(x, w, b, y, M, N, K, split_k, stream)
+
+
+def poot_linear_gemm_plan(M: int, N: int, K: int, sm_count: int = 152):
+    """(status, plan dict) of the GEMM's automatic tile plan (host only)."""
+    p = GemmPlan()
+    rc = load_library().poot_linear_gemm_plan(M, N, K, sm_count, ctypes.byref(p))
+    return rc, {n: getattr(p, n) for n, _ in GemmPlan._fields_}
 
 
 def poot_linear_tp_shard(extent: int, world: int, rank: int):

@@ -814,12 +814,14 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
     const bool few = tiles < 4 * int64_t(st.sm_count);
     a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
     constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
+    // 9 <= M <= 16 always on eight warps: sixteen warps of the two-column-
+    // block kernel need about 80 registers each, one block per SM, so 256
+    // tiles took two waves (16 x 4096 x 4096 on GB300: 14.6 us against 9.2)
     if (M <= 8)
       e = few ? launch(gemv_f16_mma_kernel<1, WF>, mgrid, dim3(WF * 32), 0, stream, a)
               : launch(gemv_f16_mma_kernel<1, WM>, mgrid, dim3(WM * 32), 0, stream, a);
     else
-      e = few ? launch(gemv_f16_mma_kernel<2, WF>, mgrid, dim3(WF * 32), 0, stream, a)
-              : launch(gemv_f16_mma_kernel<2, WM>, mgrid, dim3(WM * 32), 0, stream, a);
+      e = launch(gemv_f16_mma_kernel<2, WM>, mgrid, dim3(WM * 32), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV) {
     e = launch_gemv_mt<true>(mt, dim3(static_cast<unsigned>(blocks)), smem, stream, a);
   } else {
@@ -888,12 +890,12 @@ int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const 
         e = few ? launch(gemv_f16_mma_kernel<1, WF, kEpiF16, true>, grid, block, 0, stream, a)
                 : launch(gemv_f16_mma_kernel<1, WM, kEpiF16, true>, grid, block, 0, stream, a);
     } else {
+      // eight warps for 9 <= M <= 16 (see launch_gemv)
+      const dim3 block8(WM * 32);
       if (bf)
-        e = few ? launch(gemv_f16_mma_kernel<2, WF, kEpiBf16, true>, grid, block, 0, stream, a)
-                : launch(gemv_f16_mma_kernel<2, WM, kEpiBf16, true>, grid, block, 0, stream, a);
+        e = launch(gemv_f16_mma_kernel<2, WM, kEpiBf16, true>, grid, block8, 0, stream, a);
       else
-        e = few ? launch(gemv_f16_mma_kernel<2, WF, kEpiF16, true>, grid, block, 0, stream, a)
-                : launch(gemv_f16_mma_kernel<2, WM, kEpiF16, true>, grid, block, 0, stream, a);
+        e = launch(gemv_f16_mma_kernel<2, WM, kEpiF16, true>, grid, block8, 0, stream, a);
     }
   }
   return e == cudaSuccess ? POOT_OK : cuda_fail(e);
@@ -1186,6 +1188,21 @@ int poot_contract_grouped(const void* x, const void* w, const void* b, void* y, 
 int poot_linear_f16_splitk_noalloc(const void* x, const void* w, const void* b, void* y, int64_t M, int64_t N,
                                    int64_t K, int split_k, poot_stream_t stream) {
   return run_splitk_noalloc(x, w, b, y, M, N, K, split_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int poot_linear_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, poot_gemm_plan* out) {
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim || sm_count < 2 || out == nullptr)
+    return POOT_ERR_INVALID_ARG;
+  const GemmPlan p = plan_gemm(M, N, K, sm_count, 0, 0, 0, 0, 0, true, true);
+  const int64_t bm = p.pair ? 2 * kGemmBM : kGemmBM;
+  std::memset(out, 0, sizeof(*out));
+  out->tile_n = p.bn;
+  out->cluster = p.cluster;
+  out->split_k = p.split;
+  out->k_chunk = p.chunk_kb * kGemmBK;
+  out->tiles = static_cast<int>(((M + bm - 1) / bm) * ((N + p.bn - 1) / p.bn) * p.split);
+  out->ctas = p.pair ? 2 * (sm_count / 2) : sm_count;
+  return POOT_OK;
 }
 
 int poot_linear_tp_shard(int64_t extent, int world, int rank, int64_t* begin, int64_t* end) {

@@ -32,7 +32,7 @@ def test_library_builds_and_loads():
 
 def test_every_declared_symbol_is_exported_and_bound():
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 14, names
     lib = L.load_library()
     for n in names:
         assert hasattr(lib, n), n
