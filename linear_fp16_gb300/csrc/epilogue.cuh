@@ -124,15 +124,87 @@ __device__ __forceinline__ float ep_activation(int op, float t, int dt) {
   }
 }
 
-// The activation OP over n packed pairs of head-dtype values, in place.
-// Unrolled so that several elements' dependent chains (exp, divide, the
-// roundings) are in flight at once.
+// ---- packed pairs ------------------------------------------------------------
+// Two head-dtype values in one 32-bit word (low = first).  Add and multiply
+// of such pairs are the IEEE operations of the head dtype, rounded to
+// nearest even (the correctly rounded result, the same value as the FP32
+// operation followed by one rounding), two lanes of work per instruction;
+// the _rn forms keep the compiler from contracting a multiply and an add
+// into one fused (singly rounded) operation.  Division goes through the
+// IEEE FP32 division and one rounding.
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_add(uint32_t a, uint32_t b) {
+  if constexpr (DT == kEpiBf16) {
+    const __nv_bfloat162 r = __hadd2_rn(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                        *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  } else {
+    const __half2 r = __hadd2_rn(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_mul(uint32_t a, uint32_t b) {
+  if constexpr (DT == kEpiBf16) {
+    const __nv_bfloat162 r = __hmul2_rn(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                        *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  } else {
+    const __half2 r = __hmul2_rn(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_div(uint32_t a, uint32_t b) {
+  const float2 fa = ep_unpack_t<DT>(a), fb = ep_unpack_t<DT>(b);
+  return ep_pack_t<DT>(__fdiv_rn(fa.x, fb.x), __fdiv_rn(fa.y, fb.y));
+}
+// a constant in both halves, rounded to the head dtype
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_const(float c) {
+  return ep_pack_t<DT>(c, c);
+}
+// ADD / MUL step on a pair of head values and a pair of operand values
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_binop(int op, uint32_t t, uint32_t r) {
+  return op == kEpAdd ? ep_h2_add<DT>(t, r) : ep_h2_mul<DT>(t, r);
+}
+// exp of the negated pair: both evaluated in FP32 (expf), rounded
+template <int DT>
+__device__ __forceinline__ uint32_t ep_h2_exp_neg(uint32_t z) {
+  const float2 f = ep_unpack_t<DT>(z);
+  return ep_pack_t<DT>(expf(-f.x), expf(-f.y));  // -z is exact
+}
+
+// The activation OP over n packed pairs of head-dtype values, in place, with
+// the same primitives and roundings as ep_activation_t, two lanes at a time.
 template <int OP, int DT, int N>
 __device__ __forceinline__ void ep_activation_pairs(uint32_t* v) {
+  const uint32_t one = ep_h2_const<DT>(1.0f);
 #pragma unroll 2
   for (int i = 0; i < N; ++i) {
-    const float2 t = ep_unpack_t<DT>(v[i]);
-    v[i] = ep_pack_t<DT>(ep_activation_t<OP, DT>(t.x), ep_activation_t<OP, DT>(t.y));
+    const uint32_t t = v[i];
+    if constexpr (OP == kEpSilu) {
+      const uint32_t d = ep_h2_add<DT>(one, ep_h2_exp_neg<DT>(t));
+      v[i] = ep_h2_div<DT>(t, d);
+    } else if constexpr (OP == kEpGeluTanh) {
+      // constants as in ep_gelu_tanh_t
+      const uint32_t c1 = ep_h2_const<DT>(0.044715f), c2 = ep_h2_const<DT>(1.5957691216057308f);
+      const uint32_t sq = ep_h2_mul<DT>(t, t);
+      const uint32_t cu = ep_h2_mul<DT>(sq, t);
+      const uint32_t u = ep_h2_mul<DT>(c1, cu);
+      const uint32_t w = ep_h2_add<DT>(t, u);
+      const uint32_t z = ep_h2_mul<DT>(c2, w);
+      const uint32_t d = ep_h2_add<DT>(one, ep_h2_exp_neg<DT>(z));
+      v[i] = ep_h2_div<DT>(t, d);
+    } else {
+      const uint32_t c3 = ep_h2_const<DT>(0.70710678118654752f), half = ep_h2_const<DT>(0.5f);
+      const uint32_t sc = ep_h2_mul<DT>(c3, t);
+      const float2 sf = ep_unpack_t<DT>(sc);
+      const uint32_t e = ep_pack_t<DT>(erff(sf.x), erff(sf.y));
+      const uint32_t d = ep_h2_add<DT>(one, e);
+      v[i] = ep_h2_mul<DT>(half, ep_h2_mul<DT>(t, d));
+    }
   }
 }
 

@@ -768,12 +768,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                   const uint4 rv = ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s], row, M,
                                             nc + 8 * ch, N, args.ep_vec[s] != 0);
                   const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                  // head-dtype pair arithmetic: the correctly rounded sum
+                  // or product of two head values
 #pragma unroll
-                  for (int p2 = 0; p2 < 4; ++p2) {
-                    const float2 tv = ep_unpack(packed[4 * ch + p2], dt), r = ep_unpack(rw[p2], dt);
-                    packed[4 * ch + p2] = op == kEpAdd ? ep_pack(__fadd_rn(tv.x, r.x), __fadd_rn(tv.y, r.y), dt)
-                                                       : ep_pack(__fmul_rn(tv.x, r.x), __fmul_rn(tv.y, r.y), dt);
-                  }
+                  for (int p2 = 0; p2 < 4; ++p2)
+                    packed[4 * ch + p2] = dt == kEpiBf16 ? ep_h2_binop<kEpiBf16>(op, packed[4 * ch + p2], rw[p2])
+                                                         : ep_h2_binop<kEpiF16>(op, packed[4 * ch + p2], rw[p2]);
                 }
               } else {
                 uint32_t tmp[16];
