@@ -605,12 +605,18 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       int grp, mb, nb;
       tile_decode(t, grp, mb, nb);
       const int m0 = mb * tile_rows + (int)rank * kGemmBM, n0 = nb * BN;
-      // pull this warp's bias values into L1 now, so that the final epilogue
-      // reads them at L1 latency instead of waiting on memory once per box
+      // this warp's bias values, loaded now and used after the accumulators
+      // are ready, so that their memory latency hides behind the main loop:
+      // lane l holds b[n0 + col0 + 32g + l] for each 32-column box g
+      // (measured: loaded after the last chunk, or prefetched into L1, the
+      // first box waited about 0.4 us on them)
+      const __half* bg = args.b + (size_t)grp * N;
+      unsigned short bias16[kGemmHalfCols / 32];
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         const int col = n0 + col0 + g * 32 + lane;
-        if ((!GEN || args.has_bias) && g < ngroups && col < N) prefetch_l1(args.b + (size_t)grp * N + col);
+        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(__ldg(bg + col))
+                                                                        : (unsigned short)0;
       }
       float acc[kGemmHalfCols];
 #pragma unroll
@@ -641,20 +647,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
       }
       if (!ok) break;
-      // final epilogue of this tile from registers; lane l of box g holds
-      // b[n0 + col0 + 32g + l], all boxes loaded together (the plain
-      // epilogue reads whole aligned boxes as broadcast vectors instead)
-      // this tile's group: its bias and output (step operands below)
-      const __half* bg = args.b + (size_t)grp * N;
+      // final epilogue of this tile from registers; this tile's group: its
+      // output (step operands below)
       __half* yg = args.y + (size_t)grp * M * N;
-      unsigned short bias16[kGemmHalfCols / 32];
-#pragma unroll
-      for (int g = 0; g < kGemmHalfCols / 32; ++g) {
-        const int nc = n0 + col0 + g * 32, col = nc + lane;
-        const bool bvec = !GEN && nc + 32 <= N && (reinterpret_cast<uintptr_t>(bg + nc) & 15u) == 0;
-        bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N && !bvec) ? __half_as_ushort(bg[col])
-                                                                                  : (unsigned short)0;
-      }
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         if (g < ngroups) {
@@ -723,22 +718,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           }
           uint32_t packed[16];
           if constexpr (!GEN) {
-            // b[nc .. nc+31] as 16 column pairs: four 16-byte loads of the
-            // same address by every lane (one broadcast request each) when
-            // the box is whole and aligned, else by shuffles of bias16
+            // b[nc .. nc+31] as 16 column pairs, gathered from the lanes:
+            // lane 2i + 1 sends its value up 16 bits to lane 2i first, so
+            // each pair needs one broadcast shuffle
+            const uint32_t up = (uint32_t)__shfl_down_sync(0xffffffffu, blu, 1);
+            const uint32_t pairw = (uint32_t)blu | (up << 16);
             uint32_t bw[16];
-            if (nc + 32 <= N && (reinterpret_cast<uintptr_t>(bg + nc) & 15u) == 0) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(bg + nc) + j);
-                bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                bw[i] = (uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i) |
-                        ((uint32_t)__shfl_sync(0xffffffffu, blu, 2 * i + 1) << 16);
-            }
+            for (int i = 0; i < 16; ++i) bw[i] = (uint32_t)__shfl_sync(0xffffffffu, pairw, 2 * i);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               // proj = RN16(acc) for two columns, then y = RN16(proj + b)
