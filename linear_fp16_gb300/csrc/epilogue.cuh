@@ -18,6 +18,8 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace poot {
 
 enum EpiDtype : int { kEpiF16 = 0, kEpiBf16 = 1 };
@@ -268,6 +270,26 @@ __device__ __forceinline__ uint4 ep_load8(const uint16_t* __restrict__ base, lon
   }
   r.x = w[0]; r.y = w[1]; r.z = w[2]; r.w = w[3];
   return r;
+}
+
+// Row `lane` of a 32 x 32 box of an [M, ld] operand (columns c0 .. c0+31),
+// copied by cp.async into a 32 x 64-byte shared-memory box with the 64-byte
+// swizzle of the output staging boxes (16-byte chunk j of a row at position
+// j ^ ((row >> 1) & 3), so that a warp's 16-byte accesses are free of bank
+// conflicts); zero outside [M) x [N).  The operand must be 16-byte aligned
+// with ld % 8 == 0 (c0 a multiple of 8).
+__device__ __forceinline__ void ep_operand_box_async(uint32_t box, const uint16_t* __restrict__ base, long long ld,
+                                                     int row, int M, int c0, int N, int lane) {
+  const bool rok = row < M;
+  const uint16_t* p = base + (size_t)(rok ? row : 0) * (size_t)ld + c0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = c0 + 8 * j;
+    const int n = rok ? max(0, min(8, N - c)) : 0;  // elements of this chunk inside the operand
+    cp_async_16(box + (uint32_t)(lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)), n > 0 ? (const void*)(p + 8 * j)
+                                                                                       : (const void*)base,
+                (uint32_t)(2 * n));
+  }
 }
 
 }  // namespace poot

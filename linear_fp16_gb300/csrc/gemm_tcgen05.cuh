@@ -117,8 +117,22 @@ constexpr uint32_t kGemmTmemCols = 2 * kGemmMaxBN;  // two chunk buffers, 256 co
 constexpr int kGemmHalfCols = kGemmMaxBN / 2;        // columns per epilogue warp (max)
 
 __host__ __device__ constexpr int gemm_prod_warps(int mode) { return mode == kLoadTma ? 1 : 3; }
+// Register split of the TMA kernels.  A CTA of ten or twelve warps places
+// three warps on some SM sub-partitions, whose 16K registers then cap every
+// thread at 168: the epilogue warps, which hold a tile's FP32 sums, spilled
+// there.  The TMA kernels therefore launch twelve warps (warps 10 and 11 do
+// nothing) at 168 registers, and after the prologue the warpgroup of the
+// MMA issuer and the producer gives registers back (setmaxnreg.dec to 56)
+// while the two epilogue warpgroups take them (setmaxnreg.inc to 224):
+// 256 * 224 + 128 * 56 = 384 * 168, so the increase never waits on
+// registers that are not there (the host checks the launch count).
+constexpr int kGemmLaunchRegs = 168;
+constexpr int kGemmEpiRegs = 224;
+constexpr int kGemmCtlRegs = 56;
+static_assert(8 * 32 * kGemmEpiRegs + 4 * 32 * kGemmCtlRegs <= 12 * 32 * kGemmLaunchRegs,
+              "the register split must fit the registers the CTA is launched with");
 __host__ __device__ constexpr int gemm_threads(int mode) {
-  return (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
+  return mode == kLoadTma ? 12 * 32 : (kGemmProdWarp0 + gemm_prod_warps(mode)) * 32;
 }
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base).  The operand
@@ -356,7 +370,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
   // prologue done; global memory is touched only after the previous grid
   grid_dep_wait();
 
-  if (warp >= kGemmProdWarp0) {
+  if (warp >= kGemmMmaWarp) {
+  // the MMA issuer's and the producers' warpgroup (setmaxnreg is executed by
+  // every warp of a warpgroup together)
+  if constexpr (MODE == kLoadTma) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemmCtlRegs) : "memory");
+  if (MODE == kLoadTma && warp > kGemmProdWarp0) {
+    // warps 10 and 11 of the TMA kernels: no role
+  } else if (warp >= kGemmProdWarp0) {
     // ------------------------------------------------------------ producer
     if constexpr (MODE == kLoadTma) {
       if (lane == 0) {
@@ -491,7 +511,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         }
       }
     }
-  } else if (warp == kGemmMmaWarp) {
+  } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       const bool paired = MODE == kLoadTma && args.paired != 0;
@@ -587,7 +607,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       mbar_wait(bar_drain, 0u, nullptr);
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (MODE == kLoadTma) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGemmEpiRegs) : "memory");
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quadrant: tile rows 32q .. 32q+31
     const int h = warp >> 2;  // column half
@@ -601,6 +623,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     uint32_t buf_phase = 0;
     const int M = args.M, N = args.N;
     bool ok = true;
+    // The first ADD / MUL step (num_steps if none).  With a 16-byte aligned
+    // operand its boxes are staged by cp.async: the warp's second staging
+    // buffer holds the operand box next in line (the first box of a tile is
+    // requested when the tile starts, each next one as soon as the previous
+    // one has been read), its first buffer the output boxes.
+    int s_first = 0;
+    if constexpr (FULL) {
+      while (s_first < args.num_steps && args.ep_op[s_first] != kEpAdd && args.ep_op[s_first] != kEpMul) ++s_first;
+    }
+    const bool op_stage = FULL && s_first < args.num_steps && args.ep_vec[s_first] != 0;
     for (int t = unit; t < args.num_tiles && ok; t += units) {
       int grp, mb, nb;
       tile_decode(t, grp, mb, nb);
@@ -617,6 +649,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int col = n0 + col0 + g * 32 + lane;
         bias16[g] = ((!GEN || args.has_bias) && g < ngroups && col < N) ? __half_as_ushort(__ldg(bg + col))
                                                                         : (unsigned short)0;
+      }
+      if (op_stage) {
+        ep_operand_box_async(stg_addr + L::STG_BYTES, args.ep_ptr[s_first] + (size_t)grp * M * args.ep_ld[s_first],
+                             args.ep_ld[s_first], m0 + q * 32 + lane, M, n0 + col0, N, lane);
+        cp_async_commit();
       }
       float acc[kGemmHalfCols];
 #pragma unroll
@@ -750,10 +787,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             for (int s = 0; s < (FULL ? args.num_steps : 0); ++s) {
               const int op = args.ep_op[s];
               if (op == kEpAdd || op == kEpMul) {
+                const bool staged = op_stage && s == s_first;
+                if (staged) cp_async_wait_all();  // this lane's row of the box has landed
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                  const uint4 rv = ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s], row, M,
-                                            nc + 8 * ch, N, args.ep_vec[s] != 0);
+                  const uint4 rv =
+                      staged ? *reinterpret_cast<const uint4*>(stg + L::STG_BYTES + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4))
+                             : ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s], row, M,
+                                        nc + 8 * ch, N, args.ep_vec[s] != 0);
                   const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
                   // head-dtype pair arithmetic: the correctly rounded sum
                   // or product of two head values
@@ -761,6 +802,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                   for (int p2 = 0; p2 < 4; ++p2)
                     packed[4 * ch + p2] = dt == kEpiBf16 ? ep_h2_binop<kEpiBf16>(op, packed[4 * ch + p2], rw[p2])
                                                          : ep_h2_binop<kEpiF16>(op, packed[4 * ch + p2], rw[p2]);
+                }
+                // the row is read (its values are in use above): the next
+                // box's operand may overwrite it (each lane copies and reads
+                // only its own row)
+                if (staged && g + 1 < ngroups) {
+                  ep_operand_box_async(stg_addr + L::STG_BYTES, args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s],
+                                       args.ep_ld[s], row, M, nc + 32, N, lane);
+                  cp_async_commit();
                 }
               } else {
                 uint32_t tmp[16];
@@ -773,7 +822,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             }
           }
           if (args.tma_store) {
-            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            // this buffer's previous store has read it (one output buffer
+            // when the other stages the operand)
+            if (lane == 0) {
+              if (op_stage) bulk_wait_group_read<0>();
+              else bulk_wait_group_read<1>();
+            }
             __syncwarp();
           }
           // row `lane` of the 32 x 32 box, 64-byte swizzle: chunk j at j ^ ((row >> 1) & 3)
@@ -808,7 +862,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             }
             __syncwarp();
           }
-          sbuf ^= 1;
+          if (!op_stage) sbuf ^= 1;
         }
       }
     }

@@ -67,6 +67,15 @@ int cuda_fail(cudaError_t e) {
 
 template <int MODE, int CL, int EPI = kEpiPlain>
 cudaError_t set_gemm_attrs() {
+  if (MODE == kLoadTma) {
+    // the TMA kernels rebalance registers between warpgroups (setmaxnreg):
+    // the increase would wait forever unless the CTA is launched with the
+    // registers the split adds up to
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, gemm_f16_tcgen05_kernel<MODE, CL, EPI>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kGemmLaunchRegs) return cudaErrorInvalidKernelImage;
+  }
   return cudaFuncSetAttribute(gemm_f16_tcgen05_kernel<MODE, CL, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Layout::DYN_BYTES);
 }

@@ -215,7 +215,7 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32
                : "memory");
 }
 
-// 16 bytes, L2 only; src_bytes (0 or 16) copied, the rest zero-filled.
+// 16 bytes, L2 only; the first src_bytes (0 .. 16) copied, the rest zero-filled.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
