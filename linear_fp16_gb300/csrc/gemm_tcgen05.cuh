@@ -784,15 +784,28 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
               packed[i] = t;
             }
             const int row = m0 + q * 32 + lane;
+            // the staged operand of this box into registers, then the next
+            // box's request: it has this whole box's steps to land
+            uint4 opv[4];
+            if (op_stage) {
+              cp_async_wait_all();  // this lane's row of the box has landed
+#pragma unroll
+              for (int ch = 0; ch < 4; ++ch)
+                opv[ch] = *reinterpret_cast<const uint4*>(stg + L::STG_BYTES + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4));
+              if (g + 1 < ngroups) {
+                ep_operand_box_async(stg_addr + L::STG_BYTES, args.ep_ptr[s_first] + (size_t)grp * M * args.ep_ld[s_first],
+                                     args.ep_ld[s_first], row, M, nc + 32, N, lane);
+                cp_async_commit();
+              }
+            }
             for (int s = 0; s < (FULL ? args.num_steps : 0); ++s) {
               const int op = args.ep_op[s];
               if (op == kEpAdd || op == kEpMul) {
                 const bool staged = op_stage && s == s_first;
-                if (staged) cp_async_wait_all();  // this lane's row of the box has landed
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                   const uint4 rv =
-                      staged ? *reinterpret_cast<const uint4*>(stg + L::STG_BYTES + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4))
+                      staged ? opv[ch]
                              : ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s], row, M,
                                         nc + 8 * ch, N, args.ep_vec[s] != 0);
                   const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
@@ -802,14 +815,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                   for (int p2 = 0; p2 < 4; ++p2)
                     packed[4 * ch + p2] = dt == kEpiBf16 ? ep_h2_binop<kEpiBf16>(op, packed[4 * ch + p2], rw[p2])
                                                          : ep_h2_binop<kEpiF16>(op, packed[4 * ch + p2], rw[p2]);
-                }
-                // the row is read (its values are in use above): the next
-                // box's operand may overwrite it (each lane copies and reads
-                // only its own row)
-                if (staged && g + 1 < ngroups) {
-                  ep_operand_box_async(stg_addr + L::STG_BYTES, args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s],
-                                       args.ep_ld[s], row, M, nc + 32, N, lane);
-                  cp_async_commit();
                 }
               } else {
                 uint32_t tmp[16];
