@@ -393,6 +393,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         // barrier phase).
         const bool paired = args.paired != 0;
         const int step = paired ? 2 : 1;
+        // x tiles are marked evict-last in L2: a group of M blocks is read
+        // by every N block of its walk while W streams past it (8192 x
+        // 14336 x 4096: DRAM reads 332 -> 327 MB; prefill 81.7 -> 81.0 us)
+        const uint64_t xpol = l2_policy_evict_last();
         int ck = 0, ch = 0;
         for (int t = unit; t < args.num_tiles && ok; t += units) {
           int g, mb, nb;
@@ -427,11 +431,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 const uint32_t fb0 = map_to_cta(fb, lead_rank);
                 if (leader) mbar_arrive_expect_tx(fb, (uint32_t)(2 * STAGE_BYTES));
                 const int arow = xrow0 + mb * tile_rows + (int)rank * kGemmBM;
-                tma_load_2d_pair(stage_a(st), &tm_x, fb0, kc, arow);
+                tma_load_2d_pair_hint(stage_a(st), &tm_x, fb0, kc, arow, xpol);
                 tma_load_2d_pair(stage_b(st), &tm_w, fb0, kc, wrow0 + nb * BN + (int)rank * (BN / 2));
               } else {
                 mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-                tma_load_2d(stage_a(st), &tm_x, fb, kc, xrow0 + mb * kGemmBM);
+                tma_load_2d_hint(stage_a(st), &tm_x, fb, kc, xrow0 + mb * kGemmBM, xpol);
                 tma_load_2d(stage_b(st), &tm_w, fb, kc, wrow0 + nb * BN);
               }
             }
