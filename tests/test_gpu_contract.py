@@ -275,6 +275,33 @@ def test_strided_and_unaligned_operands():
     _check_head(x, w, b, [("add", r1.contiguous()), ("mul", r2.contiguous())], y, "f16", exact_sums=True)
 
 
+@pytest.mark.parametrize("pair,tile_n", [(1, 64), (1, 128), (2, 224), (2, 256)])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_staged_operand_boxes(pair, tile_n, dt):
+    # The first ADD / MUL step's operand, 16-byte aligned with ld % 8 == 0, is
+    # staged through shared memory box by box (cp.async); here ld = N + 4 with
+    # N % 8 == 4, so the last 16-byte chunk of each row is half inside the
+    # operand (a partial copy, zero-filled), M leaves a ragged last tile, and
+    # the tile widths give one to four boxes per epilogue warp.  A second
+    # operand step reads its operand directly.
+    M, N, K = 333, 1004, 256
+    x, w, b = _inputs(M, N, K, "smallint", 400 + tile_n, dt)
+    x, w = x / 4, w / 4
+    wide = _operand(M, N + 4, "smallint", 401, dt)
+    r1 = wide[:, :N]
+    r2 = _operand(M, N, "smallint", 402, dt)
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    wide_d, r2_d = wide.to(DEV), r2.to(DEV)
+    assert wide_d[:, :N].stride(0) % 8 == 0 and wide_d.data_ptr() % 16 == 0
+    for steps_d, steps_h in (
+            ([("add", wide_d[:, :N]), "silu", ("mul", r2_d)], [("add", r1.contiguous()), "silu", ("mul", r2)]),
+            (["gelu_tanh", ("mul", wide_d[:, :N])], ["gelu_tanh", ("mul", r1.contiguous())])):
+        y = L.contract(xd, wd, bd, steps=steps_d, gemm_cluster=pair, gemm_tile_n=tile_n).cpu()
+        torch.cuda.synchronize()
+        assert L.poot_linear_device_status(0) == L.POOT_OK
+        _check_head(x, w, b, steps_h, y, dt, exact_sums=True)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 512), (8, 1000, 770), (16, 72, 33)])
 def test_small_m_on_the_gemv_and_the_gemm(M, N, K):
     # K % 8 == 0: the GEMV with the per-element epilogue; else (and when the
