@@ -81,11 +81,9 @@ struct GemmArgs {
   int split_k;
 };
 
-// Activation step over the 16 packed pairs of one 32-column box (kept out of
-// line: the packed pairs pass through local memory only on this path).  The
-// op and dtype are dispatched once per box, so each loop body is
-// straight-line code.
-__device__ __noinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) {
+// Activation step over the 16 packed pairs of one 32-column box, the op and
+// dtype dispatched once per box, so each loop body is straight-line code.
+__device__ __forceinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) {
   if (dt == kEpiBf16) {
     switch (op) {
       case kEpSilu: ep_activation_pairs<kEpSilu, kEpiBf16, 16>(v); break;
@@ -101,6 +99,13 @@ __device__ __noinline__ void gemm_epi_activation16(uint32_t* v, int op, int dt) 
       default: break;
     }
   }
+}
+
+// The same, out of line: the copy-producer kernels (168 registers, no
+// register split) apply it box by box with the tile's sums live, and an
+// inlined copy per box would cost them registers.
+__device__ __noinline__ void gemm_epi_activation16_call(uint32_t* v, int op, int dt) {
+  gemm_epi_activation16(v, op, dt);
 }
 
 enum GemmEpi : int { kEpiPlain = 0, kEpiHead = 1, kEpiFull = 2 };
@@ -637,6 +642,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       while (s_first < args.num_steps && args.ep_op[s_first] != kEpAdd && args.ep_op[s_first] != kEpMul) ++s_first;
     }
     const bool op_stage = FULL && s_first < args.num_steps && args.ep_vec[s_first] != 0;
+    bool has_act = false;  // an activation among the steps
+    if constexpr (FULL) {
+      for (int s = 0; s < args.num_steps; ++s) has_act |= args.ep_op[s] != kEpAdd && args.ep_op[s] != kEpMul;
+    }
     for (int t = unit; t < args.num_tiles && ok; t += units) {
       int grp, mb, nb;
       tile_decode(t, grp, mb, nb);
@@ -691,6 +700,113 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       // final epilogue of this tile from registers; this tile's group: its
       // output (step operands below)
       __half* yg = args.y + (size_t)grp * M * N;
+      if constexpr (FULL && MODE == kLoadTma) {
+        if (has_act) {
+          // Epilogue steps with an activation, one box at a time in a loop
+          // that is not unrolled: the box in work is always acc[0..31] (the
+          // sums rotate by one box per iteration, register moves), so each
+          // activation is inlined once, and no call keeps the tile's sums
+          // live across it (interleaved on 8192 x 14336 x 4096: SwiGLU
+          // 786 -> 758 us, GELU tanh 780 -> 742; with K = 64, where the
+          // epilogue alone sets the time, SiLU 377 -> 359, SwiGLU 476 ->
+          // 439).  Steps without an activation keep the unrolled loop
+          // below, whose boxes overlap better (residual: 593 against 638).
+          const int dt = args.dtype;
+          const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+          for (int g = 0; g < kGemmHalfCols / 32; ++g) {
+            if (g < ngroups) {
+              const int nc = n0 + col0 + g * 32;
+              const unsigned short blu = bias16[0];
+              uint32_t packed[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                uint32_t t = ep_pack(acc[2 * i], acc[2 * i + 1], dt);
+                const float b0 = ep_widen(__shfl_sync(0xffffffffu, blu, 2 * i), dt);
+                const float b1 = ep_widen(__shfl_sync(0xffffffffu, blu, 2 * i + 1), dt);
+                if (args.has_bias) {
+                  const float2 tv = ep_unpack(t, dt);
+                  t = ep_pack(__fadd_rn(tv.x, b0), __fadd_rn(tv.y, b1), dt);
+                }
+                packed[i] = t;
+              }
+              uint4 opv[4];
+              if (op_stage) {
+                cp_async_wait_all();
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                  opv[ch] = *reinterpret_cast<const uint4*>(stg + L::STG_BYTES + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4));
+                if (g + 1 < ngroups) {
+                  ep_operand_box_async(stg_addr + L::STG_BYTES, args.ep_ptr[s_first] + (size_t)grp * M * args.ep_ld[s_first],
+                                       args.ep_ld[s_first], row, M, nc + 32, N, lane);
+                  cp_async_commit();
+                }
+              }
+              for (int s = 0; s < args.num_steps; ++s) {
+                const int op = args.ep_op[s];
+                if (op == kEpAdd || op == kEpMul) {
+                  const bool staged = op_stage && s == s_first;
+#pragma unroll
+                  for (int ch = 0; ch < 4; ++ch) {
+                    const uint4 rv = staged ? opv[ch]
+                                            : ep_load8(args.ep_ptr[s] + (size_t)grp * M * args.ep_ld[s], args.ep_ld[s],
+                                                       row, M, nc + 8 * ch, N, args.ep_vec[s] != 0);
+                    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                    for (int p2 = 0; p2 < 4; ++p2)
+                      packed[4 * ch + p2] = dt == kEpiBf16 ? ep_h2_binop<kEpiBf16>(op, packed[4 * ch + p2], rw[p2])
+                                                           : ep_h2_binop<kEpiF16>(op, packed[4 * ch + p2], rw[p2]);
+                  }
+                } else {
+                  gemm_epi_activation16(packed, op, dt);
+                }
+              }
+              if (args.tma_store) {
+                if (lane == 0) {
+                  if (op_stage) bulk_wait_group_read<0>();
+                  else bulk_wait_group_read<1>();
+                }
+                __syncwarp();
+              }
+              uint8_t* rowp = stg + sbuf * L::STG_BYTES + lane * 64;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int pos = j ^ ((lane >> 1) & 3);
+                *reinterpret_cast<uint4*>(rowp + pos * 16) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+              }
+              if (args.tma_store) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_3d(&tm_y, stg_addr + sbuf * L::STG_BYTES, nc, m0 + q * 32, grp);
+                  bulk_commit_group();
+                }
+              } else {
+                __syncwarp();
+                const uint8_t* box = stg + sbuf * L::STG_BYTES;
+                const int col = nc + lane;
+#pragma unroll 4
+                for (int rr = 0; rr < 32; ++rr) {
+                  const int r = m0 + q * 32 + rr;
+                  if (r < M && col < N) {
+                    const int pos = (lane >> 3) ^ ((rr >> 1) & 3);
+                    yg[(size_t)r * N + col] =
+                        *reinterpret_cast<const __half*>(box + rr * 64 + pos * 16 + (lane & 7) * 2);
+                  }
+                }
+                __syncwarp();
+              }
+              if (!op_stage) sbuf ^= 1;
+            }
+#pragma unroll
+            for (int i = 0; i < kGemmHalfCols - 32; ++i) acc[i] = acc[i + 32];
+#pragma unroll
+            for (int j = 0; j < kGemmHalfCols / 32 - 1; ++j) bias16[j] = bias16[j + 1];
+          }
+          continue;  // next tile
+        }
+      }
 #pragma unroll
       for (int g = 0; g < kGemmHalfCols / 32; ++g) {
         if (g < ngroups) {
@@ -821,10 +937,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                                                          : ep_h2_binop<kEpiF16>(op, packed[4 * ch + p2], rw[p2]);
                 }
               } else {
+                // the copy-producer kernels only (the TMA kernels run
+                // activations in the rotated loop above)
                 uint32_t tmp[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) tmp[i] = packed[i];
-                gemm_epi_activation16(tmp, op, dt);
+                gemm_epi_activation16_call(tmp, op, dt);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) packed[i] = tmp[i];
               }
