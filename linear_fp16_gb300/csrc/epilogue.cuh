@@ -179,11 +179,14 @@ __device__ __forceinline__ uint32_t ep_h2_exp_neg(uint32_t z) {
 }
 
 // The activation OP over n packed pairs of head-dtype values, in place, with
-// the same primitives and roundings as ep_activation_t, two lanes at a time.
+// the same primitives and roundings as ep_activation_t, two lanes at a time;
+// four pairs' chains in flight (inlined into the GEMM's rotated box loop,
+// with 224 registers: GELU tanh 726 -> 704 us on 8192 x 14336 x 4096, the
+// other forms within 2%, against two)
 template <int OP, int DT, int N>
 __device__ __forceinline__ void ep_activation_pairs(uint32_t* v) {
   const uint32_t one = ep_h2_const<DT>(1.0f);
-#pragma unroll 2
+#pragma unroll 4
   for (int i = 0; i < N; ++i) {
     const uint32_t t = v[i];
     if constexpr (OP == kEpSilu) {
