@@ -995,7 +995,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     }
     // the staging buffers must have been read before the CTA exits; the
     // stores' writes complete with the grid (a dependent kernel's
-    // grid_dep_wait sees them)
+    // grid_dep_wait sees them).  An operand box requested at a tile's start
+    // is still in flight when a wait gave up (the abort path).
+    if constexpr (FULL) cp_async_wait_all();
     if (args.tma_store && lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
