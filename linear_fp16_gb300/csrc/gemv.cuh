@@ -316,16 +316,19 @@ __global__ void __launch_bounds__(kGemvRowThreads, 8) gemv_f16_rows_kernel(const
 // that permutation these registers are exactly the A (W) and B (x^T)
 // fragments of two m16n8k16 MMAs, and no shuffles are needed.  D[n][m]
 // accumulates y^T; warps meet in shared memory in a fixed order.
-// WARPS (8 or 16) split K: up to four 16-row tiles per SM 16 warps keep
-// twice the W bytes of a tile in flight; with more tiles 8 warps are better.
-// The L2 bulk prefetch of each warp's slice pays only with few tiles (at
-// most two for every three SMs), where it adds bytes in flight; with more
-// it competes with the loads themselves.  GB300, M = 8, K = 4096, 16 warps:
-// N = 1024 4.9 us with the prefetch against 5.8 without; N = 4096 7.8 us
-// without against 8.4 with; N = 8192 14.2 us (8 warps 16.4); N = 14336 with
-// 8 warps 20.6 us (16 warps 22.2).
+// WARPS (8 or 16) split K: below two 16-row tiles per SM 16 warps keep
+// twice the W bytes of a tile in flight; with more tiles 8 warps are better
+// (GB300, M = 8, K = 4096, interleaved: N = 4096 7.15 us with 16 warps
+// against 9.55 with 8; N = 6144 12.0 against 11.4; N = 8192 13.3 against
+// 13.0; N = 14336 22.2 against 20.6).  The L2 bulk prefetch of each warp's
+// slice pays only with few tiles (at most two for every three SMs), where
+// it adds bytes in flight; with more it competes with the loads themselves
+// (16 warps: N = 1024 4.9 us with the prefetch against 5.8 without; N =
+// 4096 7.8 us without against 8.4 with).
 constexpr int kGemvMmaWarpsFew = 16;
 constexpr int kGemvMmaWarpsMany = 8;
+// the 16-warp form for fewer than two 16-row tiles per SM
+inline bool gemv_mma_few_tiles(long long tiles, int sm_count) { return tiles < 2LL * sm_count; }
 
 __device__ __forceinline__ void mma_16816_f16_f32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                   uint32_t a3, uint32_t b0, uint32_t b1) {

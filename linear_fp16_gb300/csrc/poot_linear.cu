@@ -816,11 +816,11 @@ int launch_gemv(int variant, const DeviceState& st, const void* x, const void* w
       e = launch(gemv_f16_rows_kernel<2>, rgrid, dim3(kGemvRowThreads), 0, stream, a);
   } else if (variant == POOT_VARIANT_GEMV && wpr_req == 0) {
     // 3 <= M <= 16 on the tensor cores, 16 rows of W per block; 16 warps
-    // along K up to four such blocks per SM, the L2 prefetch up to two
+    // along K below two such blocks per SM, the L2 prefetch up to two
     // blocks for every three SMs
     const int64_t tiles = (N + 15) / 16;
     const dim3 mgrid(static_cast<unsigned>(tiles));
-    const bool few = tiles < 4 * int64_t(st.sm_count);
+    const bool few = gemv_mma_few_tiles(tiles, st.sm_count);
     a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
     constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
     // 9 <= M <= 16 always on eight warps: sixteen warps of the two-column-
@@ -887,7 +887,7 @@ int launch_gemv_wide(const DeviceState& st, const void* x, const void* w, const 
     // (16-row tiles per group)
     const int64_t tiles = G * ((N + 15) / 16);
     const dim3 grid(static_cast<unsigned>(tiles));
-    const bool few = tiles < 4 * int64_t(st.sm_count);
+    const bool few = gemv_mma_few_tiles(tiles, st.sm_count);
     a.prefetch = 3 * tiles <= 2 * int64_t(st.sm_count) ? 1 : 0;
     constexpr int WF = kGemvMmaWarpsFew, WM = kGemvMmaWarpsMany;
     const dim3 block((few ? WF : WM) * 32);
